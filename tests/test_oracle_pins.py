@@ -1,0 +1,268 @@
+"""Pins of the fp64 oracle against facts fixed outside of it.
+
+Each test ties one oracle function to something other than its own formula:
+finite differences of the loss, a textbook or library routine, a closed form
+of the Newton-Schulz iteration on a matrix of known SVD, invariants of the
+renormalisation, and special cases of the two update orders. They run on the
+CPU only.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import lact_oracle as O
+
+RNG = np.random.default_rng(20250529)
+
+
+def _tiny(d=4, dh=8, n=7, seed=0):
+    g = np.random.default_rng(seed)
+    W1 = g.normal(size=(dh, d)) / math.sqrt(d)
+    W2 = g.normal(size=(d, dh)) / math.sqrt(dh)
+    W3 = g.normal(size=(dh, d)) / math.sqrt(d)
+    K = g.normal(size=(n, d))
+    V = g.normal(size=(n, d))
+    eta = 0.01 * np.log1p(np.exp(g.normal(size=n))) + 0.05
+    return W1, W2, W3, K, V, eta
+
+
+# ---------------------------------------------------------------- silu pieces
+def test_silu_matches_library_sigmoid():
+    x = np.linspace(-30, 30, 1001)
+    np.testing.assert_allclose(O.silu(x), x * scipy.special.expit(x), rtol=1e-14, atol=1e-300)
+    np.testing.assert_allclose(O.sigmoid(x), scipy.special.expit(x), rtol=1e-14, atol=1e-300)
+
+
+def test_silu_grad_is_derivative_of_silu():
+    x = np.linspace(-8, 8, 321)
+    h = 1e-6
+    fd = (x + h) * scipy.special.expit(x + h) - (x - h) * scipy.special.expit(x - h)
+    np.testing.assert_allclose(O.silu_grad(x), fd / (2 * h), rtol=1e-8, atol=1e-9)
+
+
+# ------------------------------------------------------------------ readout
+def test_apply_matches_elementwise_loops():
+    W1, W2, W3, K, _, _ = _tiny(d=3, dh=5, n=4, seed=1)
+    out = O.fast_weight_apply(W1, W2, W3, K)
+    for i in range(K.shape[0]):
+        for j in range(W2.shape[0]):
+            acc = 0.0
+            for r in range(W1.shape[0]):
+                h1 = sum(W1[r, c] * K[i, c] for c in range(K.shape[1]))
+                h3 = sum(W3[r, c] * K[i, c] for c in range(K.shape[1]))
+                acc += W2[j, r] * (h1 / (1.0 + math.exp(-h1))) * h3
+            assert abs(out[i, j] - acc) < 1e-12
+
+
+def test_apply_permutation_case_by_hand():
+    # W1 = diag(s) P, W3 = R (permutation), W2 = T (permutation), d = dh = 3:
+    # o_j = silu(s_r q_{P(r)}) q_{R(r)} with r = T^{-1}(j).
+    q = np.array([0.3, -1.2, 2.0])
+    s = np.array([1.5, -0.5, 2.0])
+    P = np.eye(3)[[2, 0, 1]]
+    R = np.eye(3)[[1, 2, 0]]
+    T = np.eye(3)[[1, 0, 2]]
+    o = O.fast_weight_apply(np.diag(s) @ P, T, R, q[None, :])[0]
+    h1 = s * q[[2, 0, 1]]
+    u = h1 * scipy.special.expit(h1) * q[[1, 2, 0]]
+    np.testing.assert_allclose(o, u[[1, 0, 2]], rtol=1e-14)
+
+
+def test_apply_zero_gate_matrix_gives_zero():
+    W1, W2, W3, K, _, _ = _tiny(seed=2)
+    assert np.all(O.fast_weight_apply(W1, W2, np.zeros_like(W3), K) == 0.0)
+
+
+# ----------------------------------------------------------------- gradient
+@pytest.mark.parametrize("seed", [3, 4])
+def test_gradient_matches_central_differences(seed):
+    W1, W2, W3, K, V, eta = _tiny(seed=seed)
+    g = O.chunk_gradient(W1, W2, W3, K, V, eta)
+    Ws = [W1, W2, W3]
+    h = 1e-6
+    for m in range(3):
+        fd = np.zeros_like(Ws[m])
+        for idx in np.ndindex(Ws[m].shape):
+            plus = [w.copy() for w in Ws]
+            minus = [w.copy() for w in Ws]
+            plus[m][idx] += h
+            minus[m][idx] -= h
+            fd[idx] = (O.chunk_loss(*plus, K, V, eta) - O.chunk_loss(*minus, K, V, eta)) / (2 * h)
+        err = np.max(np.abs(fd - g[m])) / np.max(np.abs(g[m]))
+        assert err < 1e-7, (m, err)
+
+
+def test_gradient_single_token_closed_form():
+    W1, W2, W3, K, V, eta = _tiny(n=1, seed=5)
+    k, v, e = K[0], V[0], eta[0]
+    h1, h3 = W1 @ k, W3 @ k
+    sg = scipy.special.expit(h1)
+    u = h1 * sg * h3
+    back = W2.T @ v                        # W2^T v
+    dW2 = -e * np.outer(v, u)
+    dW1 = -e * np.outer(back * h3 * sg * (1 + h1 * (1 - sg)), k)
+    dW3 = -e * np.outer(back * h1 * sg, k)
+    g = O.chunk_gradient(W1, W2, W3, K, V, eta)
+    for a, b in zip(g, (dW1, dW2, dW3)):
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-15)
+
+
+def test_gradient_is_sum_over_tokens_and_linear_in_eta():
+    W1, W2, W3, K, V, eta = _tiny(n=9, seed=6)
+    g = O.chunk_gradient(W1, W2, W3, K, V, eta)
+    parts = [O.chunk_gradient(W1, W2, W3, K[i:i + 1], V[i:i + 1], eta[i:i + 1]) for i in range(9)]
+    for m in range(3):
+        np.testing.assert_allclose(g[m], sum(p[m] for p in parts), rtol=1e-12, atol=1e-15)
+    g3 = O.chunk_gradient(W1, W2, W3, K, V, 3.0 * eta)
+    for m in range(3):
+        np.testing.assert_allclose(g3[m], 3.0 * g[m], rtol=1e-12, atol=1e-15)
+    g0 = O.chunk_gradient(W1, W2, W3, K, np.zeros_like(V), eta)
+    assert all(np.all(x == 0.0) for x in g0)
+
+
+# ------------------------------------------------------------- bf16 rounding
+def test_bf16_round_matches_torch_conversion():
+    x = RNG.normal(size=20000).astype(np.float32) * np.float32(3.0)
+    # exact ties: an 8-bit significand plus half a unit in the last place,
+    # in [1, 2) (ulp 2**-7) and in [0.25, 0.5)
+    sig = np.arange(128, 256, dtype=np.float32)
+    ties = np.concatenate([(sig + np.float32(0.5)) / np.float32(128.0),
+                           (sig + np.float32(0.5)) / np.float32(512.0)])
+    x = np.concatenate([x, ties, -ties, np.float32([0.0, 1.0, -2.5])])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.bf16_round(x.astype(np.float64)), want)
+
+
+# ------------------------------------------------------------ Newton-Schulz
+def _scalar_ns(x, steps=5, a=O.NS_A, b=O.NS_B, c=O.NS_C):
+    for _ in range(steps):
+        x = a * x + b * x ** 3 + c * x ** 5
+    return x
+
+
+def _orth(n, g):
+    q, r = np.linalg.qr(g.normal(size=(n, n)))
+    return q * np.sign(np.diag(r))
+
+
+@pytest.mark.parametrize("shape", [(6, 10), (10, 6), (8, 8)])
+def test_newton_schulz_closed_form_on_known_svd(shape):
+    g = np.random.default_rng(7)
+    m, n = shape
+    k = min(m, n)
+    U, V = _orth(m, g), _orth(n, g)
+    s = np.sort(g.uniform(0.2, 3.0, size=k))[::-1]
+    G = U[:, :k] @ np.diag(s) @ V[:, :k].T
+    want = U[:, :k] @ np.diag(_scalar_ns(s / (np.linalg.norm(s) + O.NS_EPS))) @ V[:, :k].T
+    got = O.newton_schulz5(G, bf16_points=False)
+    np.testing.assert_allclose(got, want, atol=1e-11)
+    # with the bf16 rounding points the iteration drifts from the exact one
+    # by a few percent on small matrices (rounding of X amplified by p'(x))
+    got16 = O.newton_schulz5(G, bf16_points=True)
+    assert np.linalg.norm(got16 - want) / np.linalg.norm(want) < 8e-2
+
+
+def test_newton_schulz_diagonal_reduces_to_scalar_iteration_with_rounding():
+    s = np.array([0.9, 0.5, 0.31, 0.07, 0.02])
+    G = np.zeros((5, 7))
+    G[np.arange(5), np.arange(5)] = s
+    x = s / (np.linalg.norm(s) + O.NS_EPS)
+    r = O.bf16_round
+    for _ in range(5):
+        xr = r(x)
+        A = xr * xr
+        Bm = O.NS_B * A + O.NS_C * r(A) * r(A)
+        x = O.NS_A * x + r(Bm) * xr
+    want = np.zeros((5, 7))
+    want[np.arange(5), np.arange(5)] = x
+    np.testing.assert_array_equal(O.newton_schulz5(G, bf16_points=True), want)
+
+
+def test_newton_schulz_invariances():
+    g = np.random.default_rng(8)
+    G = g.normal(size=(5, 9))
+    P, R = _orth(5, g), _orth(9, g)
+    base = O.newton_schulz5(G, bf16_points=False)
+    np.testing.assert_allclose(O.newton_schulz5(G.T, bf16_points=False), base.T, atol=1e-12)
+    np.testing.assert_allclose(O.newton_schulz5(P @ G @ R, bf16_points=False), P @ base @ R, atol=1e-11)
+    np.testing.assert_array_equal(O.newton_schulz5(G.T), O.newton_schulz5(G).T)
+
+
+def test_newton_schulz_singular_values_in_band():
+    # The published property of these quintic coefficients: after five steps
+    # the singular values land roughly in [0.5, 1.5] rather than exactly at 1,
+    # for every normalised input singular value not too close to zero.
+    g = np.random.default_rng(9)
+    for _ in range(5):
+        G = g.normal(size=(16, 48))
+        sv_in = np.linalg.svd(G / np.linalg.norm(G), compute_uv=False)
+        assert sv_in.min() > 2e-3
+        for pts in (False, True):
+            sv = np.linalg.svd(O.newton_schulz5(G, bf16_points=pts), compute_uv=False)
+            assert sv.min() > 0.5 and sv.max() < 1.5
+
+
+# ----------------------------------------------------------- renormalisation
+def test_renorm_preserves_row_norms_and_direction():
+    g = np.random.default_rng(10)
+    W = g.normal(size=(12, 7))
+    D = 0.3 * g.normal(size=(12, 7))
+    W[3] = 0.0
+    D[3] = 0.0
+    out = O.renorm_update(W, D)
+    np.testing.assert_allclose(np.linalg.norm(out, axis=1), np.linalg.norm(W, axis=1), rtol=1e-14)
+    Wt = W + D
+    for j in range(12):
+        if j == 3:
+            assert np.all(out[j] == 0.0)
+            continue
+        cos = out[j] @ Wt[j] / (np.linalg.norm(out[j]) * np.linalg.norm(Wt[j]))
+        assert abs(cos - 1.0) < 1e-14
+    np.testing.assert_allclose(O.renorm_update(W, np.zeros_like(W)), W, rtol=1e-15)
+
+
+def test_gd_step_lowers_loss_before_renorm():
+    W1, W2, W3, K, V, eta = _tiny(n=16, seed=11)
+    eta = eta * 0.05
+    L0 = O.chunk_loss(W1, W2, W3, K, V, eta)
+    g = O.chunk_gradient(W1, W2, W3, K, V, eta)
+    L1 = O.chunk_loss(W1 - g[0], W2 - g[1], W3 - g[2], K, V, eta)
+    assert L1 < L0
+
+
+# ------------------------------------------------------------------- orders
+def test_causal_single_chunk_reads_initial_weights():
+    W1, W2, W3, K, V, eta = _tiny(n=10, seed=12)
+    Q = np.random.default_rng(13).normal(size=K.shape)
+    o, Wf = O.sequence_causal((W1, W2, W3), Q, K, V, eta, chunk=10, opt="gd")
+    np.testing.assert_array_equal(o, O.fast_weight_apply(W1, W2, W3, Q))
+    Wu = O.chunk_update((W1, W2, W3), K, V, eta, "gd")
+    for a, b in zip(Wf, Wu):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_causal_chunks_read_only_earlier_chunks():
+    W1, W2, W3, K, V, eta = _tiny(n=12, seed=14)
+    Q = np.random.default_rng(15).normal(size=K.shape)
+    o, _ = O.sequence_causal((W1, W2, W3), Q, K, V, eta, chunk=4, opt="muon")
+    np.testing.assert_array_equal(o[:4], O.fast_weight_apply(W1, W2, W3, Q[:4]))
+    W = O.chunk_update((W1, W2, W3), K[:4], V[:4], eta[:4], "muon")
+    np.testing.assert_array_equal(o[4:8], O.fast_weight_apply(*W, Q[4:8]))
+    # changing a later chunk's keys does not change earlier outputs
+    K2 = K.copy()
+    K2[8:] += 1.0
+    o2, _ = O.sequence_causal((W1, W2, W3), Q, K2, V, eta, chunk=4, opt="muon")
+    np.testing.assert_array_equal(o2[:8], o[:8])
+
+
+def test_set_mode_is_update_then_apply_and_slices_sum():
+    W1, W2, W3, K, V, eta = _tiny(n=20, seed=16)
+    Q = np.random.default_rng(17).normal(size=(5, K.shape[1]))
+    o, Wf = O.sequence_set((W1, W2, W3), Q, K, V, eta, opt="muon")
+    Wu = O.chunk_update((W1, W2, W3), K, V, eta, "muon")
+    np.testing.assert_allclose(o, O.fast_weight_apply(*Wu, Q), rtol=0, atol=0)
+    o2, W2f = O.sequence_set((W1, W2, W3), Q, K, V, eta, opt="muon", token_slice=7)
+    np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-14)
