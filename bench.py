@@ -1,0 +1,351 @@
+"""Benchmark of the LaCT fast-weight chunk step on B300 (liblact, sm_103a).
+
+One step = one whole layer call (lact_sequence) over one batch of synthetic
+input: for the million-token set workload, the chunk gradient over 1,048,576
+update tokens per head (8 heads, d=128, dh=512), one Muon step (5-step
+Newton-Schulz) with row renorm, then the readout of 65,536 query tokens.
+
+Prints ONE JSON line (rank 0). `value` is update+apply tokens/s over all
+ranks with inputs resident in HBM; `e2e` is the same metric through the
+public API with host (pinned) buffers, host<->device copies inside the timed
+region. Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (no collective in the data path: weak scaling).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+                  [--impl lact|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference there is) on
+a bounded sample of the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import lact_inputs as li  # noqa: E402
+
+METRIC = "TTT-layer tokens/sec (update+apply); tensor TFLOP/s vs B300 dense BF16 peak"
+UNIT = "tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--workload", type=int, default=5)
+    p.add_argument("--impl", default="lact", choices=["lact", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def flops(w: li.Workload) -> dict:
+    """Algorithmic FLOP of one layer call (per the method, no recompute)."""
+    BH, d, dh = w.B * w.H, w.d, w.dh
+    if w.order == "causal":
+        upd, app, chunks = 12 * d * dh * w.n_kv * BH, 6 * d * dh * w.n_q * BH, -(-w.n_kv // w.chunk)
+    else:
+        upd, app, chunks = 12 * d * dh * w.n_kv * BH, 6 * d * dh * w.n_q * BH, 1
+    m, n = min(d, dh), max(d, dh)
+    ns = (5 * (4 * m * m * n + 2 * m ** 3) * 3 * BH * chunks) if w.opt == "muon" else 0
+    return {"update": upd, "apply": app, "ns": ns, "total": upd + app + ns}
+
+
+def tokens_per_step(w: li.Workload) -> int:
+    # causal tokens are both read and used for the update: count each once
+    # (a layer token is processed by every head, so heads do not multiply it)
+    per = w.n_kv if w.order == "causal" else w.n_kv + w.n_q
+    return w.B * per
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "sm_max_mhz": 2032.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def pinned_inputs(w, inp):
+    import torch
+
+    def t(a):
+        if a.dtype == np.uint16:
+            x = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        else:
+            x = torch.from_numpy(a)
+        return x.pin_memory()
+    return t(inp.q), t(inp.k), t(inp.v), t(inp.eta)
+
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS uses (the oracle's only parallel part)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = sum(x.get("num_threads", 0) for x in threadpool_info() if x.get("user_api") == "blas")
+        if n:
+            return n
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    # OpenBLAS default: one thread per available core, capped at its build limit (64)
+    return min(len(os.sched_getaffinity(0)), 64)
+
+
+def cpu_baseline(w: li.Workload, seconds_target: float = 15.0):
+    """The oracle, as it stands, on a bounded sample of the workload: one
+    (b, h), a token sample with the workload's update:query ratio."""
+    from oracle import lact_oracle as O
+    if w.order == "causal":
+        n = min(w.n_kv, 4 * w.chunk)
+        s = w.with_tokens(n, seed=w.seed + 7)
+    else:
+        n = min(w.n_kv, 131072)
+        nq = max(1, w.n_q * n // w.n_kv)
+        s = w.with_tokens(n, n_q=nq, seed=w.seed + 7)
+    s1 = dataclasses.replace(s, B=1, H=1)
+    inp = li.make_inputs(s1)
+    t0 = time.perf_counter()
+    O.run_workload(s1, inp, token_slice=65536)
+    dt = time.perf_counter() - t0
+    threads = blas_threads()
+    toks = tokens_per_step(s1)
+    return {"value": toks / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"1 (b,h) of the workload: {s1.n_kv} update + {s1.n_q if s1.order == 'set' else 0} "
+                      f"query tokens, d={s1.d}, dh={s1.dh}, {s1.opt}, {s1.order}; fp64 numpy/OpenBLAS; "
+                      f"{dt:.2f} s; value = sample tokens / time",
+            "seconds": dt}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    res = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(w)
+        if i >= args.warmup:
+            res.append(r)
+    val = statistics.median(r["value"] for r in res)
+    ms = statistics.median(r["seconds"] for r in res) * 1e3
+    cb = dict(res[-1]); cb["value"] = val; cb.pop("seconds", None)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": cb["sample"]},
+            "cpu_baseline": cb,
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    w = li.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    rank, world, local = dist_env()
+    import torch
+    from chunk_test_step_b300 import lact as L
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg:
+            pg.barrier()
+
+    # ---- inputs: generated on the host once, resident in HBM for `value`
+    inp = li.make_inputs(w)
+    hq, hk, hv, he = pinned_inputs(w, inp)
+    q, k, v, e = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, he))
+    W1, W2, W3 = (torch.from_numpy(x).to(dev) for x in (inp.W1, inp.W2, inp.W3))
+    cfg = L.make_config(w.B, w.H, w.d, w.dh, w.dtype, w.opt, max_chunk=w.chunk, ns_steps=w.ns_steps,
+                        ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr)
+    layer = L.LactLayer(cfg, W1, W2, W3, device=dev)
+    order = L.LACT_CAUSAL_APPLY_THEN_UPDATE if w.order == "causal" else L.LACT_SET_UPDATE_THEN_APPLY
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    def step():
+        L.lact_sequence(layer.handle, order, q, w.n_q, k, v, e, w.n_kv, w.chunk, o, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = L.lact_sync_status(layer.handle)
+    if st != L.LACT_OK:
+        raise RuntimeError(f"device status after warm-up: {L.lact_status_str(st)}")
+
+    # ---- timed region: inputs in HBM (> L2: no flush needed)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)
+    L.lact_set_profiling(layer.handle, True)
+    n0 = L.lact_launch_count()
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = L.lact_launch_count() - n0
+    prof = L.lact_get_profile(layer.handle)
+    L.lact_set_profiling(layer.handle, False)
+    ck = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    if pg:
+        t = torch.tensor([ms_total], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    tok = tokens_per_step(w)
+    value = tok * world / (ms_step / 1e3)
+
+    # ---- e2e: host (pinned) inputs copied in, the call, the output copied out
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, he))
+    d2h = ho.numel() * ho.element_size()
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True); e.copy_(he, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    st = L.lact_sync_status(layer.handle)
+    if st != L.LACT_OK:
+        raise RuntimeError(f"device status after the timed region: {L.lact_status_str(st)}")
+
+    # ---- roofline of the dominant kernel (the fused gradient kernel)
+    pk, pk_src = peaks()
+    fl = flops(w)
+    grad = prof["grad"]
+    grad_ms = grad["ms"] / max(1, grad["launches"])
+    grad_flop = fl["update"] / (1 if w.order == "set" else -(-w.n_kv // w.chunk))
+    achieved = grad_flop / (grad_ms / 1e3) / 1e12
+    tensor = grad["tensor_launches"] > 0
+    if tensor:
+        peak, bound, note = pk["bf16_tflops"], "tensor", f"dense bf16 burst, {pk_src}"
+    else:
+        # CUDA-core fp32 FMA: 148 SMs x 128 FMA/clk x 2 FLOP x max SM clock
+        peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+        bound, note = "alu", "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": None, "kernel": "grad", "peak_source": note,
+            "ms_per_launch": grad_ms, "flop_per_launch": grad_flop}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "dh": w.dh,
+                       "update_tokens_per_head": w.n_kv, "query_tokens_per_head": w.n_q,
+                       "chunk": w.chunk, "order": w.order, "opt": w.opt,
+                       "l2": "inputs larger than L2 (no flush)",
+                       "tflops_per_s": fl["total"] / (ms_step / 1e3) / 1e12 * world},
+            "roofline": roof,
+            "e2e": {"value": tok * world / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "clocks": ck,
+            "phases_ms_per_step": {p: prof[p]["ms"] / args.steps for p in prof}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w)
+        cb.pop("seconds", None)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

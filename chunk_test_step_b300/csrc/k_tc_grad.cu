@@ -1,0 +1,408 @@
+// Fused chunk-gradient kernel on the sm_103a tensor cores (tcgen05 + TMA +
+// TMEM), bf16 io, head dim 128.
+//
+// For the loss L = -sum_i eta_i <f_W(k_i), v_i> of the SwiGLU fast-weight
+// memory f_W(x) = W2 (silu(W1 x) * (W3 x)) (LaCT review page, "Local
+// attention and nonlinear memory work together"), the chunk gradient
+// decomposes over blocks r of 64 hidden units: with K, V the chunk's keys and
+// values ([tokens, 128]) and eta the per-token rates,
+//   H1 = K W1_r^T, H3 = K W3_r^T, A = V W2[:, r]            (forward, tokens x 64)
+//   u' = -eta silu(H1) H3, du = -eta A,
+//   dh1 = du H3 silu'(H1), dh3 = du silu(H1)                (registers)
+//   dW1_r^T += K^T dh1, dW3_r^T += K^T dh3, dW2[:, r] += V^T u'   (weight gradients)
+// so one CTA owns (hidden block r, token range, head) and never exchanges
+// intermediates with another CTA. Per 128-token tile the CTA runs
+// 4 GEMMs of 128x(64|128)x128 on the tensor cores:
+//   fwd : [H1 | H3] (TMEM, 128 cols) = K . [W1_r ; W3_r]^T    (A K-major, B K-major)
+//         A        (TMEM,  64 cols) = V . W2[:, r]            (A K-major, B MN-major)
+//   grad: [dW1_r^T | dW3_r^T] (TMEM, 128 cols) += K^T . [dh1 | dh3]   (A, B MN-major)
+//         dW2[:, r]          (TMEM,  64 cols) += V^T . u'             (A, B MN-major)
+// The same TMA-loaded K and V tiles serve as K-major A operands in the
+// forward GEMMs and as MN-major A operands in the gradient GEMMs.
+//
+// Warp roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs (one thread), warps 2..9 are the epilogue (thread = token,
+// half of the 64 hidden units each), which pulls the forward accumulators
+// out of TMEM, forms dh1, dh3, u' in fp32 and writes them as bf16 into the
+// swizzled operand buffer of the gradient GEMMs. Splits over tokens write
+// fp32 partial sums that a separate kernel adds in a fixed order.
+//
+// Every mbarrier wait is bounded; a wait that gives up sets ST_TIMEOUT in the
+// status word, the CTA unwinds (draining its own TMA copies and MMAs) and
+// frees its TMEM.
+#include "lact_internal.cuh"
+#include "tc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace lact {
+
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;         // head dim served by this kernel
+constexpr int HB = 64;         // hidden units per CTA
+constexpr int TT = 128;        // tokens per tile
+constexpr int STAGES = 2;      // K/V pipeline depth
+constexpr int NTHREADS = 320;
+
+constexpr uint32_t BOX = TT * 128;                    // one [128 rows][64 bf16] swizzled box: 16 KB
+constexpr uint32_t OFF_WCAT = 0;                      // 2 k-atoms x [W1_r rows 0-63 ; W3_r rows 64-127]
+constexpr uint32_t OFF_W2 = 2 * BOX;                  // W2[:, r]: [128 d rows][64 hid]
+constexpr uint32_t OFF_KV = 3 * BOX;                  // stage s: K box0, K box1, V box0, V box1
+constexpr uint32_t KV_STAGE = 4 * BOX;
+constexpr uint32_t OFF_B = OFF_KV + STAGES * KV_STAGE;  // dh1 | dh3 | u' (each [128 tok][64 hid])
+constexpr uint32_t SMEM_TILES = OFF_B + 3 * BOX;        // 229376
+constexpr uint32_t SMEM_BYTES = SMEM_TILES + 1024;      // + alignment slack
+
+// TMEM columns
+constexpr uint32_t COL_H13 = 0;     // H1 0-63, H3 64-127
+constexpr uint32_t COL_A = 128;     // V W2_r
+constexpr uint32_t COL_DW13 = 256;  // dW1_r^T 256-319, dW3_r^T 320-383 (lanes = d)
+constexpr uint32_t COL_DW2 = 384;   // dW2[:, r] (lanes = d)
+constexpr uint32_t TMEM_COLS = 512;
+
+constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s per wait
+
+enum { B_W = 0, B_KVF = 1, B_KVE = 1 + STAGES, B_FWDF = 1 + 2 * STAGES, B_FWDE, B_BF, B_BE, B_ACC, B_DRAIN, NBARS };
+
+struct GradArgs {
+    const float* eta;      // [BH, n_total]
+    int64_t n_total;       // tokens per head in k, v, eta
+    int64_t t0;            // first token of the chunk
+    int64_t n;             // tokens in the chunk
+    int tiles_per_split;
+    int ntiles;
+    float* partial;        // [splits][3][BH][dh*d]
+    int BH;
+    int dh;
+    int* status;
+};
+
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+          const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w3,
+          const __grid_constant__ CUtensorMap tm_w2, const GradArgs a) {
+    extern __shared__ __align__(1024) unsigned char smraw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bars[NBARS];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ int skip_cta;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = blockIdx.x, split = blockIdx.y, bh = blockIdx.z;
+    const uint32_t base = smem_u32(sm);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+    const int tile_begin = split * a.tiles_per_split;
+    const int tile_end = min(a.ntiles, tile_begin + a.tiles_per_split);
+    const int count = max(0, tile_end - tile_begin);
+
+    if (tid == 0) {
+        skip_cta = (*reinterpret_cast<volatile int*>(a.status) & ST_TIMEOUT) ? 1 : 0;
+        abort_flag = 0;
+        mbar_init(bar(B_W), 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar(B_KVF + s), 1);
+            mbar_init(bar(B_KVE + s), 1);
+        }
+        mbar_init(bar(B_FWDF), 1);
+        mbar_init(bar(B_FWDE), 8);
+        mbar_init(bar(B_BF), 8);
+        mbar_init(bar(B_BE), 1);
+        mbar_init(bar(B_ACC), 1);
+        mbar_init(bar(B_DRAIN), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (skip_cta) return;   // an earlier CTA's wait gave up: results are void anyway
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    volatile int* abort_v = &abort_flag;
+    auto give_up = [&]() {
+        atomicOr(a.status, ST_TIMEOUT);
+        *abort_v = 1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_expect_tx(bar(B_W), 3 * BOX);   // [W1_r ; W3_r] (32 KB) + W2[:, r] (16 KB)
+            const int wrow = bh * a.dh + r * HB;
+            for (int at = 0; at < 2; ++at) {
+                tma_load_2d(base + OFF_WCAT + at * BOX, &tm_w1, bar(B_W), at * 64, wrow);
+                tma_load_2d(base + OFF_WCAT + at * BOX + BOX / 2, &tm_w3, bar(B_W), at * 64, wrow);
+            }
+            tma_load_2d(base + OFF_W2, &tm_w2, bar(B_W), r * HB, bh * D);
+            int issued = 0;
+            for (int i = 0; i < count && !*abort_v; ++i) {
+                const int s = i % STAGES;
+                if (i >= STAGES && !mbar_wait(bar(B_KVE + s), ((i / STAGES) - 1) & 1, WAIT_NS)) { give_up(); break; }
+                const int tok = (int)(a.t0 + (int64_t)(tile_begin + i) * TT);
+                const uint32_t st = base + OFF_KV + s * KV_STAGE;
+                mbar_expect_tx(bar(B_KVF + s), 4 * BOX);
+                tma_load_3d(st + 0 * BOX, &tm_k, bar(B_KVF + s), 0, tok, bh);
+                tma_load_3d(st + 1 * BOX, &tm_k, bar(B_KVF + s), 64, tok, bh);
+                tma_load_3d(st + 2 * BOX, &tm_v, bar(B_KVF + s), 0, tok, bh);
+                tma_load_3d(st + 3 * BOX, &tm_v, bar(B_KVF + s), 64, tok, bh);
+                issued = i + 1;
+            }
+            // drain: the copies this thread started must land before the CTA exits
+            mbar_wait(bar(B_W), 0, WAIT_NS);
+            for (int i = max(0, issued - STAGES); i < issued; ++i)
+                mbar_wait(bar(B_KVF + i % STAGES), (i / STAGES) & 1, WAIT_NS);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t i_fwd13 = idesc_bf16_f32(128, 128, 0, 0);
+            const uint32_t i_fwda = idesc_bf16_f32(128, 64, 0, 1);
+            const uint32_t i_g13 = idesc_bf16_f32(128, 128, 1, 1);
+            const uint32_t i_g2 = idesc_bf16_f32(128, 64, 1, 1);
+            bool ok = mbar_wait(bar(B_W), 0, WAIT_NS);
+            if (!ok) give_up();
+            auto grad = [&](int i) -> bool {
+                const int s = i % STAGES;
+                if (!mbar_wait(bar(B_BF), i & 1, WAIT_NS)) return false;
+                tc_fence_after();
+                const uint32_t kb = base + OFF_KV + s * KV_STAGE, vb = kb + 2 * BOX;
+                for (int j = 0; j < TT / 16; ++j) {
+                    const uint32_t acc = (i > 0 || j > 0) ? 1u : 0u;
+                    mma_bf16(tmem + COL_DW13, sdesc_sw128(kb + j * 2048, BOX, 1024),
+                             sdesc_sw128(base + OFF_B + j * 2048, BOX, 1024), i_g13, acc);
+                    mma_bf16(tmem + COL_DW2, sdesc_sw128(vb + j * 2048, BOX, 1024),
+                             sdesc_sw128(base + OFF_B + 2 * BOX + j * 2048, BOX, 1024), i_g2, acc);
+                }
+                mma_commit(bar(B_KVE + s));
+                mma_commit(bar(B_BE));
+                return true;
+            };
+            for (int i = 0; i < count && ok && !*abort_v; ++i) {
+                const int s = i % STAGES;
+                if (!mbar_wait(bar(B_KVF + s), (i / STAGES) & 1, WAIT_NS)) { give_up(); ok = false; break; }
+                if (i >= 1 && !mbar_wait(bar(B_FWDE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
+                tc_fence_after();
+                const uint32_t kb = base + OFF_KV + s * KV_STAGE, vb = kb + 2 * BOX;
+                for (int j = 0; j < D / 16; ++j) {
+                    const uint32_t ko = (j >> 2) * BOX + (j & 3) * 32;
+                    mma_bf16(tmem + COL_H13, sdesc_sw128(kb + ko, 16, 1024),
+                             sdesc_sw128(base + OFF_WCAT + ko, 16, 1024), i_fwd13, j > 0);
+                    mma_bf16(tmem + COL_A, sdesc_sw128(vb + ko, 16, 1024),
+                             sdesc_sw128(base + OFF_W2 + j * 2048, BOX, 1024), i_fwda, j > 0);
+                }
+                mma_commit(bar(B_FWDF));
+                if (i >= 1 && !grad(i - 1)) { give_up(); ok = false; break; }
+            }
+            if (ok && count > 0 && !*abort_v) {
+                if (!grad(count - 1)) give_up();
+            }
+            mma_commit(bar(B_ACC));
+            // drain: every MMA issued above has completed once this commit lands
+            mma_commit(bar(B_DRAIN));
+            mbar_wait(bar(B_DRAIN), 0, WAIT_NS);
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int q = warp & 3;                 // TMEM lane quarter of this warp
+        const int hf = (warp - 2) >> 2;         // which 32 of the 64 hidden units
+        const int row = 32 * q + lane;          // token within the tile / d index
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        unsigned char* bbuf = sm + OFF_B;
+        const float* eta_h = a.eta + (int64_t)bh * a.n_total + a.t0;
+        bool ok = true;
+        for (int i = 0; i < count; ++i) {
+            const int64_t tok = (int64_t)(tile_begin + i) * TT + row;
+            const float e = tok < a.n ? eta_h[tok] : 0.0f;
+            if (*abort_v || !mbar_wait(bar(B_FWDF), i & 1, WAIT_NS)) { give_up(); ok = false; break; }
+            tc_fence_after();
+            uint32_t h1[32], h3[32], av[32];
+            tmem_ld32(lane_base + COL_H13 + hf * 32, h1);
+            tmem_ld32(lane_base + COL_H13 + 64 + hf * 32, h3);
+            tmem_ld32(lane_base + COL_A + hf * 32, av);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_FWDE));
+            const float ne = -e;
+            uint32_t p1[16], p3[16], pu[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                float d1[2], d3[2], uu[2];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const float x1 = __uint_as_float(h1[j + t]);
+                    const float x3 = __uint_as_float(h3[j + t]);
+                    const float s = sigmoid_fast(x1);
+                    const float si = x1 * s;                       // silu(h1)
+                    const float du = __uint_as_float(av[j + t]) * ne;
+                    uu[t] = si * x3 * ne;                          // -eta u
+                    d3[t] = du * si;                               // dL/dh3
+                    d1[t] = du * x3 * fmaf(-si, s, s + si);        // du h3 silu'(h1)
+                }
+                p1[j / 2] = pack_bf16(d1[0], d1[1]);
+                p3[j / 2] = pack_bf16(d3[0], d3[1]);
+                pu[j / 2] = pack_bf16(uu[0], uu[1]);
+            }
+            if (i >= 1 && !mbar_wait(bar(B_BE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t off = sw128_offset(row, hf * 32 + c * 8);
+                *reinterpret_cast<uint4*>(bbuf + off) = make_uint4(p1[4 * c], p1[4 * c + 1], p1[4 * c + 2], p1[4 * c + 3]);
+                *reinterpret_cast<uint4*>(bbuf + BOX + off) =
+                    make_uint4(p3[4 * c], p3[4 * c + 1], p3[4 * c + 2], p3[4 * c + 3]);
+                *reinterpret_cast<uint4*>(bbuf + 2 * BOX + off) =
+                    make_uint4(pu[4 * c], pu[4 * c + 1], pu[4 * c + 2], pu[4 * c + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_BF));
+        }
+        // ---- the CTA's partial dW out of TMEM
+        if (ok && !*abort_v && mbar_wait(bar(B_ACC), 0, WAIT_NS)) {
+            tc_fence_after();
+            const size_t mat = (size_t)a.BH * a.dh * D;
+            float* part = a.partial + (size_t)split * 3 * mat + (size_t)bh * a.dh * D;
+            if (count > 0) {
+                // dW1_r^T (hf 0) or dW3_r^T (hf 1): lane = d index `row`, column = hidden unit
+                float* pm = part + (hf == 0 ? 0 : 2 * mat);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld32(lane_base + COL_DW13 + hf * 64 + half * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        pm[(size_t)(r * HB + half * 32 + j) * D + row] = __uint_as_float(v[j]);
+                }
+                uint32_t v[32];
+                tmem_ld32(lane_base + COL_DW2 + hf * 32, v);
+                tmem_wait_ld();
+                float* p2 = part + mat + (size_t)row * a.dh + r * HB + hf * 32;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(p2 + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                                     __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+            } else {
+                float* pm = part + (hf == 0 ? 0 : 2 * mat);
+                for (int j = 0; j < 64; ++j) pm[(size_t)(r * HB + j) * D + row] = 0.0f;
+                float* p2 = part + mat + (size_t)row * a.dh + r * HB + hf * 32;
+                for (int j = 0; j < 32; ++j) p2[j] = 0.0f;
+            }
+        } else if (ok) {
+            give_up();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first.
+bool make_map(CUtensorMap* m, const void* p, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+              const uint32_t* box) {
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t gd[3], gs[2];
+    cuuint32_t bx[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; }
+    for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(p), gd, gs, bx, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool grad_tc_supported(const lact_state* st) {
+    return st->cfg.io_dtype == LACT_BF16 && st->cfg.d == D && st->cfg.dh % HB == 0 && tmap_encoder() != nullptr;
+}
+
+cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots,
+                           cudaStream_t s) {
+    const int dh = st->cfg.dh, BH = st->BH;
+    CUtensorMap mk, mv, m1, m3, m2;
+    const uint64_t kv_dims[3] = {(uint64_t)D, (uint64_t)k.n_total, (uint64_t)BH};
+    const uint64_t kv_str[2] = {(uint64_t)D * 2, (uint64_t)k.n_total * D * 2};
+    const uint32_t kv_box[3] = {64, TT, 1};
+    const uint64_t vv_dims[3] = {(uint64_t)D, (uint64_t)v.n_total, (uint64_t)BH};
+    const uint64_t vv_str[2] = {(uint64_t)D * 2, (uint64_t)v.n_total * D * 2};
+    const uint64_t w13_dims[2] = {(uint64_t)D, (uint64_t)BH * dh};
+    const uint64_t w13_str[1] = {(uint64_t)D * 2};
+    const uint32_t w13_box[2] = {64, HB};
+    const uint64_t w2_dims[2] = {(uint64_t)dh, (uint64_t)BH * D};
+    const uint64_t w2_str[1] = {(uint64_t)dh * 2};
+    const uint32_t w2_box[2] = {64, D};
+    if (!make_map(&mk, k.p, 3, kv_dims, kv_str, kv_box) || !make_map(&mv, v.p, 3, vv_dims, vv_str, kv_box) ||
+        !make_map(&m1, st->Wsh[0], 2, w13_dims, w13_str, w13_box) ||
+        !make_map(&m3, st->Wsh[2], 2, w13_dims, w13_str, w13_box) ||
+        !make_map(&m2, st->Wsh[1], 2, w2_dims, w2_str, w2_box))
+        return cudaErrorInvalidValue;
+
+    const int ntiles = (int)((k.n + TT - 1) / TT);
+    const int units = BH * (dh / HB);
+    // One CTA per SM. Token splits: at most kMaxSlots, at least 16 tiles per
+    // CTA, and, where possible, a CTA count that fills whole waves.
+    int splits = ntiles / 16;
+    if (splits > kMaxSlots) splits = kMaxSlots;
+    if (splits < 1) splits = 1;
+    for (int sp = splits; sp >= 1; --sp)
+        if (((int64_t)units * sp) % st->num_sms == 0) { splits = sp; break; }
+    const int tps = (ntiles + splits - 1) / splits;
+    splits = (ntiles + tps - 1) / tps;
+
+    GradArgs ga;
+    ga.eta = eta;
+    ga.n_total = k.n_total;
+    ga.t0 = k.t0;
+    ga.n = k.n;
+    ga.tiles_per_split = tps;
+    ga.ntiles = ntiles;
+    ga.partial = static_cast<float*>(st->partial);
+    ga.BH = BH;
+    ga.dh = dh;
+    ga.status = st->status;
+    cudaError_t e = cudaFuncSetAttribute(k_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(dh / HB, splits, BH);
+    k_grad_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(mk, mv, m1, m3, m2, ga);
+    g_launches++;
+    g_tc_launches++;
+    *slots = splits;
+    return cudaGetLastError();
+}
+
+}  // namespace lact

@@ -1,0 +1,421 @@
+// C ABI of liblact (declared in include/lact.h): argument checking, the
+// workspace, the order of the phases, per-phase timing, and dispatch to the
+// kernels.
+//
+// Orders (LaCT review page, "Update order must respect the task"):
+//   causal: per chunk, read the memory with the current W, then update W;
+//   set:    update W on all input tokens (one optimiser step), then read.
+#include "lact_internal.cuh"
+
+#include <new>
+#include <string.h>
+
+namespace lact {
+
+std::atomic<int64_t> g_launches{0};
+std::atomic<int64_t> g_tc_launches{0};
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static bool config_ok(const lact_config* c) {
+    if (!c) return false;
+    if (c->B < 1 || c->H < 1 || c->B > 65535 || c->H > 65535) return false;
+    if ((int64_t)c->B * c->H > 65535) return false;
+    if (!(c->d == 32 || c->d == 64 || c->d == 128 || c->d == 256)) return false;
+    if (c->dh < 64 || c->dh > 1024 || c->dh % 64 != 0) return false;
+    if (c->io_dtype != LACT_F32 && c->io_dtype != LACT_BF16) return false;
+    if (c->opt != LACT_OPT_GD && c->opt != LACT_OPT_MUON) return false;
+    if (c->opt == LACT_OPT_MUON && (c->ns_steps < 1 || c->ns_steps > 16)) return false;
+    if (c->max_chunk < 1 || c->max_chunk > (1LL << 40)) return false;
+    return true;
+}
+
+// Internal real type: fp64 for fp32 io, fp32 for bf16 io.
+static size_t real_size(const lact_config& c) { return c.io_dtype == LACT_F32 ? 8 : 4; }
+
+WsLayout ws_layout(const lact_config& c) {
+    WsLayout L;
+    const size_t BH = (size_t)c.B * c.H;
+    const size_t mat = BH * c.d * c.dh;
+    const size_t rs = real_size(c);
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    for (int m = 0; m < 3; ++m) L.W[m] = take(mat * rs);
+    for (int m = 0; m < 3; ++m) L.Wsh[m] = take(c.io_dtype == LACT_BF16 ? mat * 2 : 0);
+    for (int m = 0; m < 3; ++m) L.dW[m] = take(mat * rs);
+    L.partial = take((size_t)kMaxSlots * 3 * mat * rs);
+    const size_t mm = (size_t)(c.d < c.dh ? c.d : c.dh);
+    const size_t nn = (size_t)(c.d < c.dh ? c.dh : c.d);
+    L.ns[0] = take(3 * BH * mm * nn * rs);
+    L.ns[1] = take(3 * BH * mm * nn * rs);
+    L.ns[2] = take(3 * BH * mm * mm * rs);
+    L.ns[3] = take(3 * BH * mm * mm * rs);
+    L.status = take(64 * 4);
+    L.total = off;
+    return L;
+}
+
+// --------------------------------------------------------------- profiling
+static cudaEvent_t get_event(lact_state* st) {
+    if (!st->event_pool.empty()) {
+        cudaEvent_t e = st->event_pool.back();
+        st->event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Records a start event on construction and an end event on done().
+struct PhaseTimer {
+    lact_state* st;
+    cudaStream_t s;
+    int phase;
+    cudaEvent_t a = nullptr;
+    int64_t l0, t0;
+    PhaseTimer(lact_state* st_, int ph, cudaStream_t s_) : st(st_), s(s_), phase(ph) {
+        l0 = g_launches.load();
+        t0 = g_tc_launches.load();
+        if (st->profiling) {
+            a = get_event(st);
+            if (a) cudaEventRecord(a, s);
+        }
+    }
+    void done() {
+        if (!a) return;
+        cudaEvent_t b = get_event(st);
+        if (!b) { st->event_pool.push_back(a); a = nullptr; return; }
+        cudaEventRecord(b, s);
+        st->pending.push_back(PhaseEvents{a, b, phase, (int)(g_launches.load() - l0), (int)(g_tc_launches.load() - t0)});
+        a = nullptr;
+    }
+};
+
+static void drain_profile(lact_state* st) {
+    for (auto& p : st->pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(p.b) == cudaSuccess && cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+            st->prof.ms[p.phase] += ms;
+            st->prof.launches[p.phase] += p.launches;
+            st->prof.calls[p.phase] += 1;
+            st->prof.tensor_launches[p.phase] += p.tensor_launches;
+        }
+        st->event_pool.push_back(p.a);
+        st->event_pool.push_back(p.b);
+    }
+    st->pending.clear();
+}
+
+// ------------------------------------------------------------------ phases
+static lact_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LACT_OK : LACT_ERR_CUDA; }
+
+static lact_status do_apply(lact_state* st, TokView q, void* o, cudaStream_t s) {
+    if (q.n == 0) return LACT_OK;
+    PhaseTimer t(st, LACT_PHASE_APPLY, s);
+    cudaError_t e = launch_apply_simt(st, q, o, s);
+    t.done();
+    return cuda_status(e);
+}
+
+// Chunk gradient of tokens [k.t0, k.t0 + k.n) into out[] (accumulate: add to it).
+static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* eta, bool accumulate,
+                           void* const out[3], cudaStream_t s) {
+    if (k.n == 0) {
+        if (!accumulate) {
+            const size_t bytes = (size_t)st->BH * st->cfg.d * st->cfg.dh * st->rsize;
+            for (int m = 0; m < 3; ++m)
+                if (cudaMemsetAsync(out[m], 0, bytes, s) != cudaSuccess) return LACT_ERR_CUDA;
+        }
+        return LACT_OK;
+    }
+    int slots = 0;
+    {
+        PhaseTimer t(st, LACT_PHASE_GRAD, s);
+        cudaError_t e = launch_grad_simt(st, k, v, eta, &slots, s);
+        t.done();
+        if (e != cudaSuccess) return LACT_ERR_CUDA;
+    }
+    PhaseTimer t(st, LACT_PHASE_REDUCE, s);
+    cudaError_t e = launch_reduce(st, slots, accumulate, out, s);
+    t.done();
+    return cuda_status(e);
+}
+
+// Optimiser step + renorm from the gradient in g[] (Muon overwrites g[]).
+static lact_status do_step(lact_state* st, void* const g[3], cudaStream_t s) {
+    double scale = -1.0;
+    if (st->cfg.opt == LACT_OPT_MUON) {
+        PhaseTimer t(st, LACT_PHASE_NS, s);
+        cudaError_t e = launch_newton_schulz(st, g, s);
+        t.done();
+        if (e != cudaSuccess) return LACT_ERR_CUDA;
+        scale = -st->cfg.muon_lr;
+    }
+    PhaseTimer t(st, LACT_PHASE_UPDATE, s);
+    const void* gc[3] = {g[0], g[1], g[2]};
+    cudaError_t e = launch_update(st, gc, scale, s);
+    t.done();
+    return cuda_status(e);
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace lact
+
+using namespace lact;
+
+extern "C" {
+
+size_t lact_workspace_bytes(const lact_config* cfg) {
+    if (!config_ok(cfg)) return 0;
+    return ws_layout(*cfg).total;
+}
+
+lact_status lact_init_state(lact_state** out, const lact_config* cfg, void* d_ws, size_t ws_bytes,
+                            const float* d_W1, const float* d_W2, const float* d_W3, cudaStream_t s) {
+    if (!out || !config_ok(cfg) || !d_ws || !d_W1 || !d_W2 || !d_W3) return LACT_ERR_INVALID_ARG;
+    if (((uintptr_t)d_ws & 255u) != 0 || !aligned16(d_W1) || !aligned16(d_W2) || !aligned16(d_W3))
+        return LACT_ERR_INVALID_ARG;
+    WsLayout L = ws_layout(*cfg);
+    if (ws_bytes < L.total) return LACT_ERR_INVALID_ARG;
+    lact_state* st = new (std::nothrow) lact_state();
+    if (!st) return LACT_ERR_CUDA;
+    st->cfg = *cfg;
+    st->BH = cfg->B * cfg->H;
+    st->f64 = cfg->io_dtype == LACT_F32;
+    st->rsize = real_size(*cfg);
+    st->ws = static_cast<char*>(d_ws);
+    st->ws_bytes = ws_bytes;
+    st->L = L;
+    for (int m = 0; m < 3; ++m) {
+        st->W[m] = st->ws + L.W[m];
+        st->Wsh[m] = reinterpret_cast<bf16*>(st->ws + L.Wsh[m]);
+        st->dW[m] = st->ws + L.dW[m];
+    }
+    st->partial = st->ws + L.partial;
+    for (int i = 0; i < 4; ++i) st->ns[i] = st->ws + L.ns[i];
+    st->status = reinterpret_cast<int*>(st->ws + L.status);
+    st->last_stream = s;
+    st->profiling = false;
+    memset(&st->prof, 0, sizeof(st->prof));
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        delete st;
+        return LACT_ERR_CUDA;
+    }
+    // Per-head initial weights copied to every batch entry.
+    const size_t per_head = (size_t)cfg->d * cfg->dh;
+    const float* src[3] = {d_W1, d_W2, d_W3};
+    cudaError_t e = cudaMemsetAsync(st->status, 0, 64 * 4, s);
+    for (int m = 0; m < 3 && e == cudaSuccess; ++m)
+        for (int b = 0; b < cfg->B && e == cudaSuccess; ++b)
+            e = launch_convert(src[m], false, static_cast<char*>(st->W[m]) + (size_t)b * cfg->H * per_head * st->rsize,
+                               st->f64, (size_t)cfg->H * per_head, st->num_sms, s);
+    if (e == cudaSuccess) e = launch_shadow(st, s);
+    if (e != cudaSuccess) {
+        delete st;
+        return LACT_ERR_CUDA;
+    }
+    *out = st;
+    return LACT_OK;
+}
+
+static lact_status check_io(const lact_state* st, const void* p, int64_t n) {
+    if (!st) return LACT_ERR_INVALID_ARG;
+    if (n < 0) return LACT_ERR_INVALID_ARG;
+    if (n > 0 && (!p || !aligned16(p))) return LACT_ERR_INVALID_ARG;
+    return LACT_OK;
+}
+
+lact_status lact_chunk_apply(lact_state* st, const void* d_q, int64_t n_q, void* d_o, cudaStream_t s) {
+    lact_status r = check_io(st, d_q, n_q);
+    if (r == LACT_OK) r = check_io(st, d_o, n_q);
+    if (r != LACT_OK) return r;
+    st->last_stream = s;
+    return do_apply(st, TokView{d_q, n_q, 0, n_q}, d_o, s);
+}
+
+static lact_status check_update(const lact_state* st, const void* k, const void* v, const float* eta, int64_t n) {
+    lact_status r = check_io(st, k, n);
+    if (r == LACT_OK) r = check_io(st, v, n);
+    if (r == LACT_OK) r = check_io(st, eta, n);
+    if (r != LACT_OK) return r;
+    if (n > st->cfg.max_chunk) return LACT_ERR_INVALID_ARG;
+    return LACT_OK;
+}
+
+lact_status lact_chunk_update(lact_state* st, const void* d_k, const void* d_v, const float* d_eta,
+                              int64_t n_tok, cudaStream_t s) {
+    lact_status r = check_update(st, d_k, d_v, d_eta, n_tok);
+    if (r != LACT_OK) return r;
+    st->last_stream = s;
+    r = do_grad(st, TokView{d_k, n_tok, 0, n_tok}, TokView{d_v, n_tok, 0, n_tok}, d_eta, false, st->dW, s);
+    if (r != LACT_OK) return r;
+    return do_step(st, st->dW, s);
+}
+
+lact_status lact_chunk_gradient(lact_state* st, const void* d_k, const void* d_v, const float* d_eta,
+                                int64_t n_tok, float* d_dW1, float* d_dW2, float* d_dW3, cudaStream_t s) {
+    lact_status r = check_update(st, d_k, d_v, d_eta, n_tok);
+    if (r != LACT_OK) return r;
+    if (!d_dW1 || !d_dW2 || !d_dW3 || !aligned16(d_dW1) || !aligned16(d_dW2) || !aligned16(d_dW3))
+        return LACT_ERR_INVALID_ARG;
+    st->last_stream = s;
+    r = do_grad(st, TokView{d_k, n_tok, 0, n_tok}, TokView{d_v, n_tok, 0, n_tok}, d_eta, false, st->dW, s);
+    if (r != LACT_OK) return r;
+    float* out[3] = {d_dW1, d_dW2, d_dW3};
+    const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
+    for (int m = 0; m < 3; ++m)
+        if (launch_convert(st->dW[m], st->f64, out[m], false, n, st->num_sms, s) != cudaSuccess) return LACT_ERR_CUDA;
+    return LACT_OK;
+}
+
+lact_status lact_apply_gradient(lact_state* st, const float* d_dW1, const float* d_dW2, const float* d_dW3,
+                                cudaStream_t s) {
+    if (!st || !d_dW1 || !d_dW2 || !d_dW3 || !aligned16(d_dW1) || !aligned16(d_dW2) || !aligned16(d_dW3))
+        return LACT_ERR_INVALID_ARG;
+    st->last_stream = s;
+    // The Muon step works in place, so take a copy into the state's own buffer.
+    const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
+    const float* src[3] = {d_dW1, d_dW2, d_dW3};
+    for (int m = 0; m < 3; ++m)
+        if (launch_convert(src[m], false, st->dW[m], st->f64, n, st->num_sms, s) != cudaSuccess) return LACT_ERR_CUDA;
+    return do_step(st, st->dW, s);
+}
+
+lact_status lact_sequence(lact_state* st, lact_order order, const void* d_q, int64_t n_q, const void* d_k,
+                          const void* d_v, const float* d_eta, int64_t n_kv, int64_t chunk, void* d_o,
+                          cudaStream_t s) {
+    if (!st) return LACT_ERR_INVALID_ARG;
+    if (order != LACT_CAUSAL_APPLY_THEN_UPDATE && order != LACT_SET_UPDATE_THEN_APPLY) return LACT_ERR_INVALID_ARG;
+    if (chunk < 1 || chunk > st->cfg.max_chunk) return LACT_ERR_INVALID_ARG;
+    lact_status r = check_io(st, d_q, n_q);
+    if (r == LACT_OK) r = check_io(st, d_o, n_q);
+    if (r == LACT_OK) r = check_io(st, d_k, n_kv);
+    if (r == LACT_OK) r = check_io(st, d_v, n_kv);
+    if (r == LACT_OK) r = check_io(st, d_eta, n_kv);
+    if (r != LACT_OK) return r;
+    st->last_stream = s;
+    if (order == LACT_CAUSAL_APPLY_THEN_UPDATE) {
+        if (n_q != n_kv) return LACT_ERR_INVALID_ARG;
+        for (int64_t t0 = 0; t0 < n_kv; t0 += chunk) {
+            const int64_t n = n_kv - t0 < chunk ? n_kv - t0 : chunk;
+            r = do_apply(st, TokView{d_q, n_q, t0, n}, d_o, s);
+            if (r != LACT_OK) return r;
+            r = do_grad(st, TokView{d_k, n_kv, t0, n}, TokView{d_v, n_kv, t0, n}, d_eta, false, st->dW, s);
+            if (r != LACT_OK) return r;
+            r = do_step(st, st->dW, s);
+            if (r != LACT_OK) return r;
+        }
+        return LACT_OK;
+    }
+    // set: gradients of all slices summed, one optimiser step, then readout
+    if (n_kv == 0) {
+        r = do_grad(st, TokView{d_k, n_kv, 0, 0}, TokView{d_v, n_kv, 0, 0}, d_eta, false, st->dW, s);
+    }
+    for (int64_t t0 = 0; t0 < n_kv && r == LACT_OK; t0 += chunk) {
+        const int64_t n = n_kv - t0 < chunk ? n_kv - t0 : chunk;
+        r = do_grad(st, TokView{d_k, n_kv, t0, n}, TokView{d_v, n_kv, t0, n}, d_eta, t0 > 0, st->dW, s);
+    }
+    if (r != LACT_OK) return r;
+    r = do_step(st, st->dW, s);
+    if (r != LACT_OK) return r;
+    return do_apply(st, TokView{d_q, n_q, 0, n_q}, d_o, s);
+}
+
+lact_status lact_get_weights(const lact_state* st, float* d_W1, float* d_W2, float* d_W3, cudaStream_t s) {
+    if (!st || !d_W1 || !d_W2 || !d_W3) return LACT_ERR_INVALID_ARG;
+    const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
+    float* dst[3] = {d_W1, d_W2, d_W3};
+    for (int m = 0; m < 3; ++m)
+        if (launch_convert(st->W[m], st->f64, dst[m], false, n, st->num_sms, s) != cudaSuccess) return LACT_ERR_CUDA;
+    return LACT_OK;
+}
+
+lact_status lact_set_weights(lact_state* st, const float* d_W1, const float* d_W2, const float* d_W3,
+                             cudaStream_t s) {
+    if (!st || !d_W1 || !d_W2 || !d_W3 || !aligned16(d_W1) || !aligned16(d_W2) || !aligned16(d_W3))
+        return LACT_ERR_INVALID_ARG;
+    st->last_stream = s;
+    const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
+    const float* src[3] = {d_W1, d_W2, d_W3};
+    for (int m = 0; m < 3; ++m)
+        if (launch_convert(src[m], false, st->W[m], st->f64, n, st->num_sms, s) != cudaSuccess) return LACT_ERR_CUDA;
+    return cuda_status(launch_shadow(st, s));
+}
+
+size_t lact_state_bytes(const lact_state* st) {
+    if (!st) return 0;
+    return 3 * (size_t)st->BH * st->cfg.d * st->cfg.dh * st->rsize;
+}
+
+lact_status lact_export_state(const lact_state* st, void* d_dst, size_t bytes, cudaStream_t s) {
+    if (!st || !d_dst || bytes < lact_state_bytes(st)) return LACT_ERR_INVALID_ARG;
+    const size_t one = lact_state_bytes(st) / 3;
+    for (int m = 0; m < 3; ++m)
+        if (cudaMemcpyAsync(static_cast<char*>(d_dst) + m * one, st->W[m], one, cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+            return LACT_ERR_CUDA;
+    return LACT_OK;
+}
+
+lact_status lact_import_state(lact_state* st, const void* d_src, size_t bytes, cudaStream_t s) {
+    if (!st || !d_src || bytes != lact_state_bytes(st)) return LACT_ERR_INVALID_ARG;
+    st->last_stream = s;
+    const size_t one = bytes / 3;
+    for (int m = 0; m < 3; ++m)
+        if (cudaMemcpyAsync(st->W[m], static_cast<const char*>(d_src) + m * one, one, cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+            return LACT_ERR_CUDA;
+    return cuda_status(launch_shadow(st, s));
+}
+
+lact_status lact_sync_status(lact_state* st) {
+    if (!st) return LACT_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(st->last_stream) != cudaSuccess) return LACT_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LACT_ERR_CUDA;
+    if (word & ST_TIMEOUT) return LACT_ERR_TIMEOUT;
+    if (word & ST_NONFINITE) return LACT_ERR_NONFINITE;
+    return LACT_OK;
+}
+
+lact_status lact_set_profiling(lact_state* st, int enable) {
+    if (!st) return LACT_ERR_INVALID_ARG;
+    drain_profile(st);
+    memset(&st->prof, 0, sizeof(st->prof));
+    st->profiling = enable != 0;
+    return LACT_OK;
+}
+
+lact_status lact_get_profile(lact_state* st, lact_profile* out) {
+    if (!st || !out) return LACT_ERR_INVALID_ARG;
+    drain_profile(st);
+    *out = st->prof;
+    return LACT_OK;
+}
+
+int64_t lact_launch_count(void) { return g_launches.load(); }
+
+const char* lact_status_str(lact_status s) {
+    switch (s) {
+        case LACT_OK: return "ok";
+        case LACT_ERR_INVALID_ARG: return "invalid argument";
+        case LACT_ERR_UNSUPPORTED: return "unsupported configuration";
+        case LACT_ERR_CUDA: return "CUDA error";
+        case LACT_ERR_TIMEOUT: return "device-side wait timed out";
+        case LACT_ERR_NONFINITE: return "non-finite fast-weight row norm";
+    }
+    return "unknown status";
+}
+
+void lact_free_state(lact_state* st) {
+    if (!st) return;
+    drain_profile(st);
+    for (cudaEvent_t e : st->event_pool) cudaEventDestroy(e);
+    delete st;
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+// Internal declarations of liblact: state, workspace layout, kernel entry
+// points and small device helpers. Not part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <atomic>
+#include <vector>
+
+#include "../../include/lact.h"
+
+namespace lact {
+
+typedef __nv_bfloat16 bf16;
+
+// Sticky device status bits (workspace word 0).
+enum : int { ST_NONFINITE = 1, ST_TIMEOUT = 2 };
+
+// Device workspace, carved by ws_layout() in 256-byte aligned sections.
+// "real" is the state's internal type: fp32 for bf16 io, fp64 for fp32 io.
+struct WsLayout {
+    size_t W[3];       // real master fast weights: W1 [BH,dh,d], W2 [BH,d,dh], W3 [BH,dh,d]
+    size_t Wsh[3];     // bf16 shadows of the same, same layouts (bf16 io only)
+    size_t dW[3];      // real chunk gradients (Muon: overwritten by NS output), same layouts
+    size_t partial;    // real split-K partials [kMaxSlots][3][BH][dh*d]
+    size_t ns[4];      // real Newton-Schulz scratch: X, X', A, B over 3*BH matrices
+    size_t status;     // int32[64]: [0] sticky status bits, [1..] diagnostics
+    size_t total;
+};
+
+constexpr int kMaxSlots = 64;   // split-K partial slots
+
+WsLayout ws_layout(const lact_config& c);
+
+struct PhaseEvents { cudaEvent_t a, b; int phase; int launches; int tensor_launches; };
+
+}  // namespace lact
+
+struct lact_state {
+    lact_config cfg;
+    int BH;
+    bool f64;                 // internal arithmetic in fp64 (fp32 io) or fp32 (bf16 io)
+    size_t rsize;             // bytes of one internal real
+    char* ws;
+    size_t ws_bytes;
+    lact::WsLayout L;
+    void* W[3];
+    lact::bf16* Wsh[3];
+    void* dW[3];
+    void* partial;
+    void* ns[4];
+    int* status;
+    cudaStream_t last_stream;
+    bool profiling;
+    std::vector<lact::PhaseEvents> pending;
+    std::vector<cudaEvent_t> event_pool;
+    lact_profile prof;
+    int num_sms;
+};
+
+namespace lact {
+
+extern std::atomic<int64_t> g_launches;      // every kernel launch of this library
+extern std::atomic<int64_t> g_tc_launches;   // launches of tcgen05 tensor-core kernels
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// Load an io element widened to the internal real type R.
+template <typename R> __device__ __forceinline__ R ld_io(const float* p, int64_t i) { return (R)p[i]; }
+template <typename R> __device__ __forceinline__ R ld_io(const bf16* p, int64_t i) { return (R)__bfloat162float(p[i]); }
+// Store a real as an io element (round to nearest even).
+__device__ __forceinline__ void st_io(float* p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_io(float* p, int64_t i, double x) { p[i] = (float)x; }
+__device__ __forceinline__ void st_io(bf16* p, int64_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+
+// Round to the nearest bf16 value (8 significant bits, ties to even), kept
+// in the same type. The fp64 form rounds the fp64 value directly (no
+// intermediate fp32 rounding).
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ double round_bf16(double x) {
+    unsigned long long b = (unsigned long long)__double_as_longlong(x);
+    const unsigned long long drop = 45;                 // 52 - 7 fraction bits
+    const unsigned long long lsb = (b >> drop) & 1ull;
+    b += (1ull << (drop - 1)) - 1ull + lsb;
+    b &= ~((1ull << drop) - 1ull);
+    return __longlong_as_double((long long)b);
+}
+
+__device__ __forceinline__ float fma_r(float a, float b, float c) { return fmaf(a, b, c); }
+__device__ __forceinline__ double fma_r(double a, double b, double c) { return fma(a, b, c); }
+__device__ __forceinline__ float exp_r(float x) { return expf(x); }
+__device__ __forceinline__ double exp_r(double x) { return exp(x); }
+__device__ __forceinline__ float sqrt_r(float x) { return sqrtf(x); }
+__device__ __forceinline__ double sqrt_r(double x) { return sqrt(x); }
+
+// Token-slice view of a [BH, n_total, d] tensor: tokens [t0, t0 + n) of each head.
+struct TokView {
+    const void* p;      // base of the whole tensor
+    int64_t n_total;    // tokens per head in the tensor
+    int64_t t0;         // first token of the slice
+    int64_t n;          // tokens in the slice
+};
+
+// ---------------------------------------------------------------- launchers
+// SIMT path (fp32 or bf16 io, any supported d, dh). Each returns a CUDA error.
+cudaError_t launch_apply_simt(const lact_state* st, TokView q, void* o, cudaStream_t s);
+cudaError_t launch_grad_simt(const lact_state* st, TokView k, TokView v, const float* eta,
+                             int* slots_used, cudaStream_t s);
+// Tensor-core (tcgen05) path: bf16 io, d = 128, dh a multiple of 64.
+bool grad_tc_supported(const lact_state* st);
+cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots_used,
+                           cudaStream_t s);
+cudaError_t launch_reduce(const lact_state* st, int slots, bool accumulate, void* const out[3],
+                          cudaStream_t s);
+cudaError_t launch_newton_schulz(const lact_state* st, void* const g[3], cudaStream_t s);
+cudaError_t launch_update(const lact_state* st, const void* const g[3], double scale, cudaStream_t s);
+cudaError_t launch_shadow(const lact_state* st, cudaStream_t s);
+// Element conversion between the API's fp32 buffers and internal reals.
+cudaError_t launch_convert(const void* src, bool src_f64, void* dst, bool dst_f64, size_t n, int num_sms,
+                           cudaStream_t s);
+
+}  // namespace lact

@@ -1,0 +1,225 @@
+"""GPU parity: liblact (through its C ABI) against the fp64 oracle on the same
+seeded inputs. Max relative L2 error per tensor per (b, h) must stay within
+1e-4 for fp32 workloads and 2e-2 for bf16 workloads.
+
+Sizes span several tiles with ragged tails; each row of the hot path
+(readout, chunk gradient, optimiser + renorm) is also checked on its own.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import lact_inputs as li
+from oracle import lact_oracle as O
+from tests.harness import TOL, compare, config_for, max_rel_l2_per_head, rel_l2, run_gpu, to_device, to_host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _torch():
+    import torch
+    assert torch.cuda.is_available()
+    return torch
+
+
+def _layer(w, inp, max_chunk=None):
+    from chunk_test_step_b300 import lact as L
+    return L.LactLayer(config_for(w, max_chunk), to_device(inp.W1), to_device(inp.W2), to_device(inp.W3))
+
+
+# Reduced token counts of each workload: several tiles and a ragged tail.
+SMALL = {
+    1: dict(n_kv=2048),                       # the whole tiny workload
+    2: dict(n_kv=2 * 2048 + 301),             # two full chunks + a partial one
+    3: dict(n_kv=2048),
+    4: dict(n_kv=5000 + 13, n_q=333),
+    5: dict(n_kv=8192 + 77, n_q=500),
+}
+
+
+def _small(num):
+    w = li.WORKLOADS[num]
+    return w.with_tokens(seed=w.seed + 1000, **SMALL[num])
+
+
+# ------------------------------------------------------------- row a1: readout
+@pytest.mark.parametrize("num", [1, 2, 4])
+def test_apply_matches_oracle(num):
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = _small(num)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    q = to_device(inp.q)
+    o = torch.empty_like(q)
+    L.lact_chunk_apply(layer.handle, q, w.n_q, o)
+    got = to_host_f64(o)
+    want = np.zeros_like(got)
+    for b in range(w.B):
+        for h in range(w.H):
+            want[b, h] = O.fast_weight_apply(inp.W1[h].astype(np.float64), inp.W2[h].astype(np.float64),
+                                             inp.W3[h].astype(np.float64), li.as_f64(inp.q[b, h]))
+    err = max_rel_l2_per_head(got, want)
+    assert err < TOL[w.dtype], err
+
+
+# ---------------------------------------------------- rows a2-a4: gradient
+@pytest.mark.parametrize("num,n", [(1, 1000 + 37), (2, 2048 + 5), (4, 4096 + 99), (5, 3 * 128 + 1)])
+def test_chunk_gradient_matches_oracle(num, n):
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[num].with_tokens(n, seed=li.WORKLOADS[num].seed + 2000)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp, max_chunk=n)
+    k, v, e = to_device(inp.k), to_device(inp.v), to_device(inp.eta)
+    g = [torch.empty(w.B, w.H, *s, device="cuda") for s in ((w.dh, w.d), (w.d, w.dh), (w.dh, w.d))]
+    L.lact_chunk_gradient(layer.handle, k, v, e, n, *g)
+    got = [to_host_f64(x) for x in g]
+    for b in range(w.B):
+        for h in range(w.H):
+            want = O.chunk_gradient(inp.W1[h].astype(np.float64), inp.W2[h].astype(np.float64),
+                                    inp.W3[h].astype(np.float64), li.as_f64(inp.k[b, h]),
+                                    li.as_f64(inp.v[b, h]), inp.eta[b, h].astype(np.float64))
+            for m in range(3):
+                err = rel_l2(got[m][b, h], want[m])
+                assert err < TOL[w.dtype], (m, b, h, err)
+
+
+# ------------------------------------------- rows a5-a7: optimiser + renorm
+@pytest.mark.parametrize("num,opt", [(1, "gd"), (3, "muon"), (4, "muon"), (2, "gd")])
+def test_apply_gradient_matches_oracle(num, opt):
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[num].with_tokens(128, seed=li.WORKLOADS[num].seed + 3000)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    # gradients drawn by the generator at the scale of real chunk gradients
+    s = w.seed + 3000
+    G = [li.normal(s, 20 + m, (w.B, w.H) + sh, scale=0.05)
+         for m, sh in enumerate(((w.dh, w.d), (w.d, w.dh), (w.dh, w.d)))]
+    L.lact_apply_gradient(layer.handle, *(to_device(x) for x in G))
+    got = layer.weights()
+    torch.cuda.synchronize()
+    got = [to_host_f64(x) for x in got]
+    W0 = (inp.W1, inp.W2, inp.W3)
+    for b in range(w.B):
+        for h in range(w.H):
+            for m in range(3):
+                delta = O.optimizer_delta(G[m][b, h].astype(np.float64), opt, lr=w.muon_lr)
+                want = O.renorm_update(W0[m][h].astype(np.float64), delta)
+                err = rel_l2(got[m][b, h], want)
+                assert err < TOL[w.dtype], (m, b, h, err)
+                # row norms are those before the update
+                np.testing.assert_allclose(np.linalg.norm(got[m][b, h], axis=1),
+                                           np.linalg.norm(W0[m][h].astype(np.float64), axis=1), rtol=2e-6)
+
+
+# ------------------------------------------------- whole layer calls (a8)
+@pytest.mark.parametrize("num", [1, 2, 3, 4, 5])
+def test_sequence_matches_oracle(num):
+    w = _small(num)
+    inp = li.make_inputs(w)
+    got = run_gpu(w, inp)
+    want = O.run_workload(w, inp)
+    errs = compare(w, got, want)
+    assert max(errs.values()) < TOL[w.dtype], errs
+
+
+def test_set_mode_slices_sum_before_one_step():
+    w = li.WORKLOADS[4].with_tokens(3000, n_q=100, seed=77)
+    w = dataclasses.replace(w, chunk=1024)
+    inp = li.make_inputs(w)
+    got = run_gpu(w, inp)
+    want = O.run_workload(w, inp)   # set mode: one step on all 3000 tokens
+    errs = compare(w, got, want)
+    assert max(errs.values()) < TOL[w.dtype], errs
+
+
+# ------------------------------------------------------------- edge cases
+@pytest.mark.parametrize("opt", ["gd", "muon"])
+def test_empty_update_leaves_weights(opt):
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[1].with_tokens(64, opt=opt)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    z = torch.zeros(16, device="cuda")
+    L.lact_chunk_update(layer.handle, z, z, z, 0)
+    L.lact_chunk_apply(layer.handle, z, 0, z)
+    got = [to_host_f64(x) for x in layer.weights()]
+    torch.cuda.synchronize()
+    for m, W0 in enumerate((inp.W1, inp.W2, inp.W3)):
+        np.testing.assert_array_equal(got[m][0], W0.astype(np.float64))
+    assert L.lact_sync_status(layer.handle) == L.LACT_OK
+
+
+def test_update_beyond_max_chunk_is_rejected():
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[1].with_tokens(64)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp, max_chunk=64)
+    k = torch.zeros(1, 2, 65, 64, device="cuda")
+    e = torch.zeros(1, 2, 65, device="cuda")
+    with pytest.raises(L.LactError) as ex:
+        L.lact_chunk_update(layer.handle, k, k, e, 65)
+    assert ex.value.status == L.LACT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("num", [3, 2])
+def test_checkpoint_resume_equals_one_run(num):
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[num].with_tokens(1024, chunk=256)
+    inp = li.make_inputs(w)
+    q, k, v, e = (to_device(x) for x in (inp.q, inp.k, inp.v, inp.eta))
+    one = _layer(w, inp)
+    o_one = one.sequence(L.LACT_CAUSAL_APPLY_THEN_UPDATE, q, k, v, e, 256)
+    W_one = one.weights()
+    # first half, export, a fresh state imports, second half
+    a = _layer(w, inp)
+    qa, ka, va, ea = (x[:, :, :512].contiguous() for x in (q, k, v, e))
+    o_a = a.sequence(L.LACT_CAUSAL_APPLY_THEN_UPDATE, qa, ka, va, ea, 256)
+    saved = torch.empty(L.lact_state_bytes(a.handle), dtype=torch.uint8, device="cuda")
+    L.lact_export_state(a.handle, saved)
+    b = _layer(w, inp)
+    L.lact_import_state(b.handle, saved)
+    qb, kb, vb, eb = (x[:, :, 512:].contiguous() for x in (q, k, v, e))
+    o_b = b.sequence(L.LACT_CAUSAL_APPLY_THEN_UPDATE, qb, kb, vb, eb, 256)
+    W_two = b.weights()
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([o_a, o_b], dim=2), o_one)
+    for x, y in zip(W_one, W_two):
+        assert torch.equal(x, y)
+
+
+def test_nonfinite_row_sets_status():
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[1].with_tokens(64)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    W1, W2, W3 = layer.weights()
+    W1[0, 0, 3, 5] = float("nan")
+    L.lact_set_weights(layer.handle, W1, W2, W3)
+    k, v, e = to_device(inp.k), to_device(inp.v), to_device(inp.eta)
+    L.lact_chunk_update(layer.handle, k, v, e, 64)
+    assert L.lact_sync_status(layer.handle) == L.LACT_ERR_NONFINITE
+
+
+def test_profiling_counts_phases():
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = _small(5)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    q, k, v, e = (to_device(x) for x in (inp.q, inp.k, inp.v, inp.eta))
+    L.lact_set_profiling(layer.handle, True)
+    n0 = L.lact_launch_count()
+    layer.sequence(L.LACT_SET_UPDATE_THEN_APPLY, q, k, v, e, w.chunk)
+    prof = L.lact_get_profile(layer.handle)
+    n1 = L.lact_launch_count()
+    assert all(prof[p]["calls"] == 1 for p in ("apply", "grad", "reduce", "ns", "update"))
+    assert sum(prof[p]["launches"] for p in prof) == n1 - n0
+    assert all(prof[p]["ms"] > 0 for p in prof)
