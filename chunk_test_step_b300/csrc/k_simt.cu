@@ -322,3 +322,58 @@ cudaError_t launch_reduce(const lact_state* st, int slots, bool accumulate, void
 }
 
 }  // namespace lact
+
+// ------------------------------------------------------------------------
+// Raw-pointer launchers of the bf16-io gradient and reduction kernels above,
+// for callers that hold no lact_state (the weights come straight from the
+// caller, the partial sums go to a buffer the caller names).
+namespace lact {
+
+namespace {
+template <int D>
+cudaError_t grad_raw_d(int dh, int BH, const float* W1, const float* W2, const float* W3, TokView k, TokView v,
+                       const float* eta, float* partial, int max_slots, int num_sms, int* slots, cudaStream_t s) {
+    constexpr int TT = Tile<float>::TT, HC = Tile<float>::HC;
+    auto kern = k_grad_simt<bf16, float, D>;
+    const size_t sm = grad_smem<float, D>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = (k.n + TT - 1) / TT;
+    const int units = BH * (dh / HC);
+    int64_t want = (4LL * num_sms + units - 1) / units;
+    int64_t splits = want < (ntiles + 7) / 8 ? want : (ntiles + 7) / 8;
+    if (splits > max_slots) splits = max_slots;
+    if (splits < 1) splits = 1;
+    const int tps = (int)((ntiles + splits - 1) / splits);
+    splits = (ntiles + tps - 1) / tps;
+    if (splits < 1) splits = 1;
+    dim3 grid((unsigned)splits, dh / HC, BH);
+    kern<<<grid, NT, sm, s>>>(k, v, eta, W1, W2, W3, dh, tps, partial, BH);
+    g_launches++;
+    *slots = (int)splits;
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_grad_simt_bf16_raw(int d, int dh, int BH, const float* W1, const float* W2, const float* W3,
+                                      TokView k, TokView v, const float* eta, float* partial, int max_slots,
+                                      int num_sms, int* slots, cudaStream_t s) {
+    switch (d) {
+        case 32: return grad_raw_d<32>(dh, BH, W1, W2, W3, k, v, eta, partial, max_slots, num_sms, slots, s);
+        case 64: return grad_raw_d<64>(dh, BH, W1, W2, W3, k, v, eta, partial, max_slots, num_sms, slots, s);
+        case 128: return grad_raw_d<128>(dh, BH, W1, W2, W3, k, v, eta, partial, max_slots, num_sms, slots, s);
+        case 256: return grad_raw_d<256>(dh, BH, W1, W2, W3, k, v, eta, partial, max_slots, num_sms, slots, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_reduce_f32_raw(const float* partial, int slots, size_t mat, float* o0, float* o1, float* o2,
+                                  int num_sms, cudaStream_t s) {
+    const size_t want = (3 * mat + 255) / 256, cap = (size_t)num_sms * 8;
+    const int blocks = (int)(want < cap ? want : cap);
+    k_reduce<float><<<blocks, 256, 0, s>>>(partial, slots, mat, false, o0, o1, o2);
+    g_launches++;
+    return cudaGetLastError();
+}
+
+}  // namespace lact

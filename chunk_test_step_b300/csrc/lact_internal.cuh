@@ -121,6 +121,12 @@ cudaError_t launch_reduce(const lact_state* st, int slots, bool accumulate, void
 cudaError_t launch_newton_schulz(const lact_state* st, void* const g[3], cudaStream_t s);
 cudaError_t launch_update(const lact_state* st, const void* const g[3], double scale, cudaStream_t s);
 cudaError_t launch_shadow(const lact_state* st, cudaStream_t s);
+// Raw-pointer forms of the bf16-io SIMT gradient and its reduction (no state).
+cudaError_t launch_grad_simt_bf16_raw(int d, int dh, int BH, const float* W1, const float* W2, const float* W3,
+                                      TokView k, TokView v, const float* eta, float* partial, int max_slots,
+                                      int num_sms, int* slots, cudaStream_t s);
+cudaError_t launch_reduce_f32_raw(const float* partial, int slots, size_t mat, float* o0, float* o1, float* o2,
+                                  int num_sms, cudaStream_t s);
 // Element conversion between the API's fp32 buffers and internal reals.
 cudaError_t launch_convert(const void* src, bool src_f64, void* dst, bool dst_f64, size_t n, int num_sms,
                            cudaStream_t s);

@@ -25,6 +25,7 @@ PHASES = ("apply", "grad", "reduce", "ns", "update")
 SYMBOLS = ("lact_workspace_bytes", "lact_init_state", "lact_chunk_apply", "lact_chunk_update",
            "lact_sequence", "lact_chunk_gradient", "lact_apply_gradient", "lact_get_weights",
            "lact_set_weights", "lact_state_bytes", "lact_export_state", "lact_import_state",
+           "lact_chunk_gradient_noalloc",
            "lact_sync_status", "lact_set_profiling", "lact_get_profile",
            "lact_launch_count", "lact_status_str", "lact_free_state")
 
@@ -75,6 +76,8 @@ def load() -> ctypes.CDLL:
     lib.lact_state_bytes.restype = ctypes.c_size_t
     lib.lact_export_state.argtypes = [vp, vp, ctypes.c_size_t, vp]
     lib.lact_import_state.argtypes = [vp, vp, ctypes.c_size_t, vp]
+    lib.lact_chunk_gradient_noalloc.argtypes = [P(lact_config), vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]
+    lib.lact_chunk_gradient_noalloc.restype = cint
     lib.lact_sync_status.argtypes = [vp]
     lib.lact_set_profiling.argtypes = [vp, cint]
     lib.lact_get_profile.argtypes = [vp, P(lact_profile)]
@@ -179,6 +182,14 @@ def lact_export_state(st: int, dst, stream=None) -> None:
 def lact_import_state(st: int, src, stream=None) -> None:
     _check(load().lact_import_state(st, _p(src), src.numel() * src.element_size(), _s(stream)),
            "lact_import_state")
+
+
+def lact_chunk_gradient_noalloc(cfg: lact_config, W1, W2, W3, k, v, eta, n_tok: int, dW1, dW2, dW3,
+                                stream=None) -> None:
+    """Chunk gradient with no state and no device allocation (see include/lact.h)."""
+    _check(load().lact_chunk_gradient_noalloc(ctypes.byref(cfg), _p(W1), _p(W2), _p(W3), _p(k), _p(v), _p(eta),
+                                              n_tok, _p(dW1), _p(dW2), _p(dW3), _s(stream)),
+           "lact_chunk_gradient_noalloc")
 
 
 def lact_sync_status(st: int) -> int:

@@ -153,6 +153,31 @@ size_t lact_state_bytes(const lact_state* st);
 lact_status lact_export_state(const lact_state* st, void* d_dst, size_t bytes, cudaStream_t stream);
 lact_status lact_import_state(lact_state* st, const void* d_src, size_t bytes, cudaStream_t stream);
 
+/* Chunk gradient without any device allocation and without a state. The
+ * method's pages have no counterpart of this call: it exists for callers that
+ * cannot allocate device memory (code running inside a host callback or an
+ * allocator hook, under a framework that owns the whole memory pool, or on a
+ * path that must not fail for lack of memory or synchronise the device), so
+ * cannot provide the workspace lact_init_state asks for.
+ *
+ * Computes what lact_chunk_gradient computes, for bf16 io only:
+ * d_dW1 [B,H,dh,d], d_dW2 [B,H,d,dh], d_dW3 [B,H,dh,d] (fp32 outputs) from
+ * the fp32 weights d_W1 [B,H,dh,d], d_W2 [B,H,d,dh], d_W3 [B,H,dh,d] and
+ * d_k, d_v [B,H,n_tok,d] bf16, d_eta [B,H,n_tok] fp32 (inputs), on the
+ * CUDA cores. Its split-K partial sums live in a 32 MiB array of static
+ * device memory inside this library, held by every GPU that loads it until
+ * the process exits; one split slot takes 12*B*H*d*dh bytes, and a problem
+ * whose slot does not fit returns LACT_ERR_UNSUPPORTED before anything runs.
+ * The first call on each device looks up that array's device address (make
+ * it before any stream capture). All calls share the array: two calls that
+ * may overlap on the GPU (other streams, other host threads) race, so order
+ * them on one stream. Nothing in it needs clearing: each call overwrites what
+ * it reads. Calls no cudaMalloc, cudaFree or other allocating routine. */
+lact_status lact_chunk_gradient_noalloc(const lact_config* cfg, const float* d_W1, const float* d_W2,
+                                        const float* d_W3, const void* d_k, const void* d_v,
+                                        const float* d_eta, int64_t n_tok, float* d_dW1, float* d_dW2,
+                                        float* d_dW3, cudaStream_t stream);
+
 /* Synchronise the state's last stream and return the sticky device status
  * (LACT_OK, LACT_ERR_TIMEOUT or LACT_ERR_NONFINITE), or LACT_ERR_CUDA. */
 lact_status lact_sync_status(lact_state* st);
