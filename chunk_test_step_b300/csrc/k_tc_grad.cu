@@ -33,7 +33,6 @@
 #include "lact_internal.cuh"
 #include "tc_ptx.cuh"
 
-#include <cudaTypedefs.h>
 
 namespace lact {
 
@@ -91,7 +90,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
           const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w3,
           const __grid_constant__ CUtensorMap tm_w2, const GradArgs a) {
-    extern __shared__ __align__(1024) unsigned char smraw[];
+    extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[NBARS];
     __shared__ uint32_t tmem_slot;
@@ -126,6 +125,7 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     __syncthreads();
     if (skip_cta) return;   // an earlier CTA's wait gave up: results are void anyway
     if (warp == 1) {
+        __syncwarp();
         tmem_alloc(smem_u32(&tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
@@ -230,7 +230,7 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         for (int i = 0; i < count; ++i) {
             const int64_t tok = (int64_t)(tile_begin + i) * TT + row;
             const float e = tok < a.n ? eta_h[tok] : 0.0f;
-            if (*abort_v || !mbar_wait(bar(B_FWDF), i & 1, WAIT_NS)) { give_up(); ok = false; break; }
+            if (*abort_v || !mbar_wait_warp(bar(B_FWDF), i & 1, WAIT_NS)) { give_up(); ok = false; break; }
             tc_fence_after();
             uint32_t h1[32], h3[32], av[32];
             tmem_ld32(lane_base + COL_H13 + hf * 32, h1);
@@ -260,7 +260,7 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 p3[j / 2] = pack_bf16(d3[0], d3[1]);
                 pu[j / 2] = pack_bf16(uu[0], uu[1]);
             }
-            if (i >= 1 && !mbar_wait(bar(B_BE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
+            if (i >= 1 && !mbar_wait_warp(bar(B_BE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t off = sw128_offset(row, hf * 32 + c * 8);
@@ -275,7 +275,7 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             if (lane == 0) mbar_arrive(bar(B_BF));
         }
         // ---- the CTA's partial dW out of TMEM
-        if (ok && !*abort_v && mbar_wait(bar(B_ACC), 0, WAIT_NS)) {
+        if (ok && !*abort_v && mbar_wait_warp(bar(B_ACC), 0, WAIT_NS)) {
             tc_fence_after();
             const size_t mat = (size_t)a.BH * a.dh * D;
             float* part = a.partial + (size_t)split * 3 * mat + (size_t)bh * a.dh * D;
@@ -312,43 +312,16 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// bf16 tensor map with 128-byte swizzle; dims/strides innermost first.
-bool make_map(CUtensorMap* m, const void* p, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-              const uint32_t* box) {
-    auto enc = tmap_encoder();
-    if (!enc) return false;
-    cuuint64_t gd[3], gs[2];
-    cuuint32_t bx[3], es[3] = {1, 1, 1};
-    for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; }
-    for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(p), gd, gs, bx, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool grad_tc_supported(const lact_state* st) {
-    return st->cfg.io_dtype == LACT_BF16 && st->cfg.d == D && st->cfg.dh % HB == 0 && tmap_encoder() != nullptr;
+    return st->cfg.io_dtype == LACT_BF16 && st->cfg.d == D && st->cfg.dh % HB == 0 && tmap_available();
 }
 
 cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots,
@@ -366,10 +339,10 @@ cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const flo
     const uint64_t w2_dims[2] = {(uint64_t)dh, (uint64_t)BH * D};
     const uint64_t w2_str[1] = {(uint64_t)dh * 2};
     const uint32_t w2_box[2] = {64, D};
-    if (!make_map(&mk, k.p, 3, kv_dims, kv_str, kv_box) || !make_map(&mv, v.p, 3, vv_dims, vv_str, kv_box) ||
-        !make_map(&m1, st->Wsh[0], 2, w13_dims, w13_str, w13_box) ||
-        !make_map(&m3, st->Wsh[2], 2, w13_dims, w13_str, w13_box) ||
-        !make_map(&m2, st->Wsh[1], 2, w2_dims, w2_str, w2_box))
+    if (!make_tmap_bf16(&mk, k.p, 3, kv_dims, kv_str, kv_box) || !make_tmap_bf16(&mv, v.p, 3, vv_dims, vv_str, kv_box) ||
+        !make_tmap_bf16(&m1, st->Wsh[0], 2, w13_dims, w13_str, w13_box) ||
+        !make_tmap_bf16(&m3, st->Wsh[2], 2, w13_dims, w13_str, w13_box) ||
+        !make_tmap_bf16(&m2, st->Wsh[1], 2, w2_dims, w2_str, w2_box))
         return cudaErrorInvalidValue;
 
     const int ntiles = (int)((k.n + TT - 1) / TT);

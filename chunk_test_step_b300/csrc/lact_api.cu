@@ -132,7 +132,8 @@ static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* et
     int slots = 0;
     {
         PhaseTimer t(st, LACT_PHASE_GRAD, s);
-        cudaError_t e = launch_grad_simt(st, k, v, eta, &slots, s);
+        cudaError_t e = grad_tc_supported(st) ? launch_grad_tc(st, k, v, eta, &slots, s)
+                                              : launch_grad_simt(st, k, v, eta, &slots, s);
         t.done();
         if (e != cudaSuccess) return LACT_ERR_CUDA;
     }

@@ -2,6 +2,7 @@
 // points and small device helpers. Not part of the public C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -112,10 +113,17 @@ struct TokView {
 cudaError_t launch_apply_simt(const lact_state* st, TokView q, void* o, cudaStream_t s);
 cudaError_t launch_grad_simt(const lact_state* st, TokView k, TokView v, const float* eta,
                              int* slots_used, cudaStream_t s);
+// TMA tensor maps (bf16, 128-byte swizzle); dims / strides innermost first.
+bool tmap_available();
+bool make_tmap_bf16(CUtensorMap* m, const void* p, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                    const uint32_t* box);
+
 // Tensor-core (tcgen05) path: bf16 io, d = 128, dh a multiple of 64.
 bool grad_tc_supported(const lact_state* st);
 cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots_used,
                            cudaStream_t s);
+bool apply_tc_supported(const lact_state* st);
+cudaError_t launch_apply_tc(const lact_state* st, TokView q, void* o, cudaStream_t s);
 cudaError_t launch_reduce(const lact_state* st, int slots, bool accumulate, void* const out[3],
                           cudaStream_t s);
 cudaError_t launch_newton_schulz(const lact_state* st, void* const g[3], cudaStream_t s);

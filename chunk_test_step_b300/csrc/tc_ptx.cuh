@@ -58,6 +58,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// Warp-uniform form: every lane waits, then the warp reconverges and agrees
+// on the outcome (so .sync.aligned instructions that follow see a converged
+// warp and a common decision).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
+    const bool ok = mbar_wait(bar, parity, budget_ns);
+    __syncwarp();
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
     asm volatile(

@@ -65,7 +65,8 @@ def test_apply_matches_oracle(num):
 
 
 # ---------------------------------------------------- rows a2-a4: gradient
-@pytest.mark.parametrize("num,n", [(1, 1000 + 37), (2, 2048 + 5), (4, 4096 + 99), (5, 3 * 128 + 1)])
+@pytest.mark.parametrize("num,n", [(1, 1000 + 37), (2, 2048 + 5), (4, 4096 + 99), (5, 3 * 128 + 1),
+                                   (4, 1), (4, 127), (5, 128), (5, 37 * 128 + 5)])
 def test_chunk_gradient_matches_oracle(num, n):
     torch = _torch()
     from chunk_test_step_b300 import lact as L
