@@ -135,17 +135,22 @@ k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (lane == 0) {
             const uint32_t i_h = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t i_o = idesc_bf16_f32(128, 128, 0, 0);
+            // descriptor bases; offsets (address / 16) are added as constants
+            const uint64_t dQ = sdesc_sw128(base + OFF_Q, 16, 1024);
+            const uint64_t dWc = sdesc_sw128(base + OFF_W, 16, 1024);
+            const uint64_t dW2 = sdesc_sw128(base + OFF_W + 2 * BOX, 16, 1024);
+            const uint64_t dU = sdesc_sw128(base + OFF_U, 16, 1024);
             bool ok = mbar_wait(bar(B_Q), 0, WAIT_NS);
             if (!ok) give_up();
             auto out_mma = [&](int r) -> bool {
                 const int s = r & 1;
                 if (!mbar_wait(bar(B_UF + s), (r >> 1) & 1, WAIT_NS)) return false;
                 tc_fence_after();
-                const uint32_t w2 = base + OFF_W + s * W_STAGE + 2 * BOX;
-                const uint32_t u = base + OFF_U + s * BOX;
+                const uint64_t wo = (uint64_t)(s * W_STAGE) >> 4, uo = (uint64_t)(s * BOX) >> 4;
+                const uint32_t first = r > 0 ? 1u : 0u;
+#pragma unroll
                 for (int j = 0; j < HB / 16; ++j)
-                    mma_bf16(tmem + COL_O, sdesc_sw128(u + j * 32, 16, 1024), sdesc_sw128(w2 + j * 32, 16, 1024), i_o,
-                             (r > 0 || j > 0) ? 1u : 0u);
+                    mma_bf16(tmem + COL_O, dU + uo + j * 2, dW2 + wo + j * 2, i_o, j > 0 ? 1u : first);
                 mma_commit(bar(B_WE + s));
                 mma_commit(bar(B_UE + s));
                 return true;
@@ -155,11 +160,12 @@ k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 if (!mbar_wait(bar(B_WF + s), (r >> 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
                 if (r >= 2 && !mbar_wait(bar(B_HE + s), ((r >> 1) - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
                 tc_fence_after();
-                const uint32_t wc = base + OFF_W + s * W_STAGE;
+                const uint64_t wo = (uint64_t)(s * W_STAGE) >> 4;
+                const uint32_t th = tmem + COL_H13 + s * 128;
+#pragma unroll
                 for (int j = 0; j < D / 16; ++j) {
-                    const uint32_t ko = (j >> 2) * BOX + (j & 3) * 32;
-                    mma_bf16(tmem + COL_H13 + s * 128, sdesc_sw128(base + OFF_Q + ko, 16, 1024),
-                             sdesc_sw128(wc + ko, 16, 1024), i_h, j > 0 ? 1u : 0u);
+                    const uint64_t ko = (uint64_t)((j >> 2) * BOX + (j & 3) * 32) >> 4;
+                    mma_bf16(th, dQ + ko, dWc + wo + ko, i_h, j > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(B_HF + s));
                 if (r >= 1 && !out_mma(r - 1)) { give_up(); ok = false; break; }
@@ -183,6 +189,8 @@ k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             tmem_ld32(lane_base + COL_H13 + s * 128 + hf * 32, h1);
             tmem_ld32(lane_base + COL_H13 + s * 128 + 64 + hf * 32, h3);
             tmem_wait_ld();
+            tmem_pin(h1);
+            tmem_pin(h3);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_HE + s));
@@ -216,6 +224,7 @@ k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 uint32_t v[32];
                 tmem_ld32(lane_base + COL_O + hf * 64 + h * 32, v);
                 tmem_wait_ld();
+                tmem_pin(v);
 #pragma unroll
                 for (int j = 0; j < 32; j += 2)
                     packed[h * 16 + j / 2] = pack_bf16(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));

@@ -176,19 +176,31 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             const uint32_t i_fwda = idesc_bf16_f32(128, 64, 0, 1);
             const uint32_t i_g13 = idesc_bf16_f32(128, 128, 1, 1);
             const uint32_t i_g2 = idesc_bf16_f32(128, 64, 1, 1);
+            // Descriptor bases; the start-address field is the low 14 bits
+            // (address / 16), so every k-step, stage and operand offset below
+            // is a constant added to a base.
+            const uint64_t dK = sdesc_sw128(base + OFF_KV, 16, 1024);       // K, V tiles, K-major
+            const uint64_t dKT = sdesc_sw128(base + OFF_KV, BOX, 1024);     // K, V tiles, MN-major
+            const uint64_t dWc = sdesc_sw128(base + OFF_WCAT, 16, 1024);    // [W1_r ; W3_r], K-major
+            const uint64_t dW2 = sdesc_sw128(base + OFF_W2, BOX, 1024);     // W2[:, r], MN-major
+            const uint64_t dDH = sdesc_sw128(base + OFF_B, BOX, 1024);      // [dh1 | dh3], MN-major
+            const uint64_t dU = sdesc_sw128(base + OFF_B + 2 * BOX, BOX, 1024);  // u', MN-major
+            constexpr uint64_t V_OFF = (2 * BOX) >> 4;
+            const uint32_t t_h13 = tmem + COL_H13, t_a = tmem + COL_A;
+            const uint32_t t_dw13 = tmem + COL_DW13, t_dw2 = tmem + COL_DW2;
             bool ok = mbar_wait(bar(B_W), 0, WAIT_NS);
             if (!ok) give_up();
             auto grad = [&](int i) -> bool {
                 const int s = i % STAGES;
                 if (!mbar_wait(bar(B_BF), i & 1, WAIT_NS)) return false;
                 tc_fence_after();
-                const uint32_t kb = base + OFF_KV + s * KV_STAGE, vb = kb + 2 * BOX;
+                const uint64_t so = (uint64_t)(s * KV_STAGE) >> 4;
+                const uint32_t first = i > 0 ? 1u : 0u;
+#pragma unroll
                 for (int j = 0; j < TT / 16; ++j) {
-                    const uint32_t acc = (i > 0 || j > 0) ? 1u : 0u;
-                    mma_bf16(tmem + COL_DW13, sdesc_sw128(kb + j * 2048, BOX, 1024),
-                             sdesc_sw128(base + OFF_B + j * 2048, BOX, 1024), i_g13, acc);
-                    mma_bf16(tmem + COL_DW2, sdesc_sw128(vb + j * 2048, BOX, 1024),
-                             sdesc_sw128(base + OFF_B + 2 * BOX + j * 2048, BOX, 1024), i_g2, acc);
+                    const uint32_t acc = j > 0 ? 1u : first;
+                    mma_bf16(t_dw13, dKT + so + j * 128, dDH + j * 128, i_g13, acc);
+                    mma_bf16(t_dw2, dKT + so + V_OFF + j * 128, dU + j * 128, i_g2, acc);
                 }
                 mma_commit(bar(B_KVE + s));
                 mma_commit(bar(B_BE));
@@ -199,13 +211,12 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!mbar_wait(bar(B_KVF + s), (i / STAGES) & 1, WAIT_NS)) { give_up(); ok = false; break; }
                 if (i >= 1 && !mbar_wait(bar(B_FWDE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
                 tc_fence_after();
-                const uint32_t kb = base + OFF_KV + s * KV_STAGE, vb = kb + 2 * BOX;
+                const uint64_t so = (uint64_t)(s * KV_STAGE) >> 4;
+#pragma unroll
                 for (int j = 0; j < D / 16; ++j) {
-                    const uint32_t ko = (j >> 2) * BOX + (j & 3) * 32;
-                    mma_bf16(tmem + COL_H13, sdesc_sw128(kb + ko, 16, 1024),
-                             sdesc_sw128(base + OFF_WCAT + ko, 16, 1024), i_fwd13, j > 0);
-                    mma_bf16(tmem + COL_A, sdesc_sw128(vb + ko, 16, 1024),
-                             sdesc_sw128(base + OFF_W2 + j * 2048, BOX, 1024), i_fwda, j > 0);
+                    const uint64_t ko = (uint64_t)((j >> 2) * BOX + (j & 3) * 32) >> 4;
+                    mma_bf16(t_h13, dK + so + ko, dWc + ko, i_fwd13, j > 0 ? 1u : 0u);
+                    mma_bf16(t_a, dK + so + V_OFF + ko, dW2 + j * 128, i_fwda, j > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(B_FWDF));
                 if (i >= 1 && !grad(i - 1)) { give_up(); ok = false; break; }
@@ -226,10 +237,21 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         unsigned char* bbuf = sm + OFF_B;
         const float* eta_h = a.eta + (int64_t)bh * a.n_total + a.t0;
+        uint32_t boff[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) boff[c] = sw128_offset(row, hf * 32 + c * 8);
         bool ok = true;
-        for (int i = 0; i < count; ++i) {
+        // eta of this thread's token, fetched two tiles ahead so the DRAM
+        // latency hides behind the work of the tiles in between
+        auto eta_of = [&](int i) -> float {
             const int64_t tok = (int64_t)(tile_begin + i) * TT + row;
-            const float e = tok < a.n ? eta_h[tok] : 0.0f;
+            return (i < count && tok < a.n) ? eta_h[tok] : 0.0f;
+        };
+        float e_next = eta_of(0), e_next2 = eta_of(1);
+        for (int i = 0; i < count; ++i) {
+            const float e = e_next;
+            e_next = e_next2;
+            e_next2 = eta_of(i + 2);
             if (*abort_v || !mbar_wait_warp(bar(B_FWDF), i & 1, WAIT_NS)) { give_up(); ok = false; break; }
             tc_fence_after();
             uint32_t h1[32], h3[32], av[32];
@@ -237,6 +259,9 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             tmem_ld32(lane_base + COL_H13 + 64 + hf * 32, h3);
             tmem_ld32(lane_base + COL_A + hf * 32, av);
             tmem_wait_ld();
+            tmem_pin(h1);
+            tmem_pin(h3);
+            tmem_pin(av);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_FWDE));
@@ -263,7 +288,7 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             if (i >= 1 && !mbar_wait_warp(bar(B_BE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const uint32_t off = sw128_offset(row, hf * 32 + c * 8);
+                const uint32_t off = boff[c];
                 *reinterpret_cast<uint4*>(bbuf + off) = make_uint4(p1[4 * c], p1[4 * c + 1], p1[4 * c + 2], p1[4 * c + 3]);
                 *reinterpret_cast<uint4*>(bbuf + BOX + off) =
                     make_uint4(p3[4 * c], p3[4 * c + 1], p3[4 * c + 2], p3[4 * c + 3]);
@@ -287,6 +312,7 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     uint32_t v[32];
                     tmem_ld32(lane_base + COL_DW13 + hf * 64 + half * 32, v);
                     tmem_wait_ld();
+                    tmem_pin(v);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         pm[(size_t)(r * HB + half * 32 + j) * D + row] = __uint_as_float(v[j]);
@@ -294,6 +320,7 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 uint32_t v[32];
                 tmem_ld32(lane_base + COL_DW2 + hf * 32, v);
                 tmem_wait_ld();
+                tmem_pin(v);
                 float* p2 = part + mat + (size_t)row * a.dh + r * HB + hf * 32;
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)

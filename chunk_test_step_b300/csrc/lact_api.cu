@@ -113,7 +113,7 @@ static lact_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LACT_O
 static lact_status do_apply(lact_state* st, TokView q, void* o, cudaStream_t s) {
     if (q.n == 0) return LACT_OK;
     PhaseTimer t(st, LACT_PHASE_APPLY, s);
-    cudaError_t e = launch_apply_simt(st, q, o, s);
+    cudaError_t e = apply_tc_supported(st) ? launch_apply_tc(st, q, o, s) : launch_apply_simt(st, q, o, s);
     t.done();
     return cuda_status(e);
 }
@@ -148,7 +148,7 @@ static lact_status do_step(lact_state* st, void* const g[3], cudaStream_t s) {
     double scale = -1.0;
     if (st->cfg.opt == LACT_OPT_MUON) {
         PhaseTimer t(st, LACT_PHASE_NS, s);
-        cudaError_t e = launch_newton_schulz(st, g, s);
+        cudaError_t e = ns_tc_supported(st) ? launch_ns_tc(st, g, s) : launch_newton_schulz(st, g, s);
         t.done();
         if (e != cudaSuccess) return LACT_ERR_CUDA;
         scale = -st->cfg.muon_lr;

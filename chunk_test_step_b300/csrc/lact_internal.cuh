@@ -122,6 +122,8 @@ bool make_tmap_bf16(CUtensorMap* m, const void* p, int rank, const uint64_t* dim
 bool grad_tc_supported(const lact_state* st);
 cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots_used,
                            cudaStream_t s);
+bool ns_tc_supported(const lact_state* st);
+cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s);
 bool apply_tc_supported(const lact_state* st);
 cudaError_t launch_apply_tc(const lact_state* st, TokView q, void* o, cudaStream_t s);
 cudaError_t launch_reduce(const lact_state* st, int slots, bool accumulate, void* const out[3],

@@ -44,11 +44,13 @@ def _small(num):
 
 
 # ------------------------------------------------------------- row a1: readout
-@pytest.mark.parametrize("num", [1, 2, 4])
-def test_apply_matches_oracle(num):
+@pytest.mark.parametrize("num,n_q", [(1, None), (2, None), (4, None), (5, 1), (5, 127), (5, 128 * 9 + 3)])
+def test_apply_matches_oracle(num, n_q):
     torch = _torch()
     from chunk_test_step_b300 import lact as L
     w = _small(num)
+    if n_q is not None:
+        w = w.with_tokens(w.n_kv, n_q=n_q)
     inp = li.make_inputs(w)
     layer = _layer(w, inp)
     q = to_device(inp.q)
