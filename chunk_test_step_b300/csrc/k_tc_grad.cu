@@ -44,6 +44,7 @@ constexpr int D = 128;         // head dim served by this kernel
 constexpr int HB = 64;         // hidden units per CTA
 constexpr int TT = 128;        // tokens per tile
 constexpr int STAGES = 2;      // K/V pipeline depth
+constexpr int PF = 6;          // tiles of K/V prefetched into L2 ahead of their load
 constexpr int NTHREADS = 320;
 
 constexpr uint32_t BOX = TT * 128;                    // one [128 rows][64 bf16] swizzled box: 16 KB
@@ -151,8 +152,20 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 tma_load_2d(base + OFF_WCAT + at * BOX + BOX / 2, &tm_w3, bar(B_W), at * 64, wrow);
             }
             tma_load_2d(base + OFF_W2, &tm_w2, bar(B_W), r * HB, bh * D);
+            // One CTA of each group of hidden blocks (r == 0) pulls the K/V
+            // tiles PF tiles ahead into L2, where the whole group finds them.
+            auto prefetch = [&](int i) {
+                if (r != 0 || i >= count) return;
+                const int tok = (int)(a.t0 + (int64_t)(tile_begin + i) * TT);
+                tma_prefetch_l2_3d(&tm_k, 0, tok, bh);
+                tma_prefetch_l2_3d(&tm_k, 64, tok, bh);
+                tma_prefetch_l2_3d(&tm_v, 0, tok, bh);
+                tma_prefetch_l2_3d(&tm_v, 64, tok, bh);
+            };
+            for (int i = 0; i < PF; ++i) prefetch(i);
             int issued = 0;
             for (int i = 0; i < count && !*abort_v; ++i) {
+                prefetch(i + PF);
                 const int s = i % STAGES;
                 if (i >= STAGES && !mbar_wait(bar(B_KVE + s), ((i / STAGES) - 1) & 1, WAIT_NS)) { give_up(); break; }
                 const int tok = (int)(a.t0 + (int64_t)(tile_begin + i) * TT);
@@ -190,10 +203,8 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             const uint32_t t_dw13 = tmem + COL_DW13, t_dw2 = tmem + COL_DW2;
             bool ok = mbar_wait(bar(B_W), 0, WAIT_NS);
             if (!ok) give_up();
-            auto grad = [&](int i) -> bool {
+            auto issue_grad = [&](int i) {
                 const int s = i % STAGES;
-                if (!mbar_wait(bar(B_BF), i & 1, WAIT_NS)) return false;
-                tc_fence_after();
                 const uint64_t so = (uint64_t)(s * KV_STAGE) >> 4;
                 const uint32_t first = i > 0 ? 1u : 0u;
 #pragma unroll
@@ -204,14 +215,9 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 mma_commit(bar(B_KVE + s));
                 mma_commit(bar(B_BE));
-                return true;
             };
-            for (int i = 0; i < count && ok && !*abort_v; ++i) {
-                const int s = i % STAGES;
-                if (!mbar_wait(bar(B_KVF + s), (i / STAGES) & 1, WAIT_NS)) { give_up(); ok = false; break; }
-                if (i >= 1 && !mbar_wait(bar(B_FWDE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
-                tc_fence_after();
-                const uint64_t so = (uint64_t)(s * KV_STAGE) >> 4;
+            auto issue_fwd = [&](int i) {
+                const uint64_t so = (uint64_t)((i % STAGES) * KV_STAGE) >> 4;
 #pragma unroll
                 for (int j = 0; j < D / 16; ++j) {
                     const uint64_t ko = (uint64_t)((j >> 2) * BOX + (j & 3) * 32) >> 4;
@@ -219,10 +225,31 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     mma_bf16(t_a, dK + so + V_OFF + ko, dW2 + j * 128, i_fwda, j > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(B_FWDF));
-                if (i >= 1 && !grad(i - 1)) { give_up(); ok = false; break; }
-            }
-            if (ok && count > 0 && !*abort_v) {
-                if (!grad(count - 1)) give_up();
+            };
+            // Issue whichever is ready first: the gradient GEMMs of tile g (its
+            // dh1, dh3, u' are written) or the forward GEMMs of tile f (its K/V
+            // have landed and the epilogue has read tile f-1 out of TMEM). A
+            // gradient never queues behind a K/V load this way.
+            int f = 0, g = 0;
+            uint64_t deadline = globaltimer_ns() + WAIT_NS;
+            while (ok && g < count && !*abort_v) {
+                bool progress = false;
+                if (g < f && mbar_probe(bar(B_BF), g & 1)) {
+                    tc_fence_after();
+                    issue_grad(g++);
+                    progress = true;
+                } else if (f < count && (f == 0 || mbar_probe(bar(B_FWDE), (f - 1) & 1)) &&
+                           mbar_probe(bar(B_KVF + f % STAGES), (f / STAGES) & 1)) {
+                    tc_fence_after();
+                    issue_fwd(f++);
+                    progress = true;
+                }
+                if (progress) {
+                    deadline = globaltimer_ns() + WAIT_NS;
+                } else {
+                    __nanosleep(32);   // leave issue slots to the epilogue warps
+                    if (globaltimer_ns() > deadline) { give_up(); ok = false; }
+                }
             }
             mma_commit(bar(B_ACC));
             // drain: every MMA issued above has completed once this commit lands
