@@ -49,6 +49,9 @@ def parse():
     p.add_argument("--impl", default="lact", choices=["lact", "reference"])
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    # smaller token counts of the same layer (for profiler captures of a small case)
+    p.add_argument("--update-tokens", type=int, default=None)
+    p.add_argument("--query-tokens", type=int, default=None)
     return p.parse_args()
 
 
@@ -159,25 +162,47 @@ def blas_threads() -> int:
     return min(len(os.sched_getaffinity(0)), 64)
 
 
-def cpu_baseline(w: li.Workload, seconds_target: float = 15.0):
-    """The oracle, as it stands, on a bounded sample of the workload: one
-    (b, h), a token sample with the workload's update:query ratio."""
-    from oracle import lact_oracle as O
+def oracle_sample(w: li.Workload, n_kv: int) -> li.Workload:
+    """One (b, h) of the workload with about n_kv update tokens (the workload's
+    update:query ratio for set layers, whole chunks for causal layers)."""
     if w.order == "causal":
-        n = min(w.n_kv, 4 * w.chunk)
+        n = max(w.chunk, min(w.n_kv, n_kv) // w.chunk * w.chunk)
         s = w.with_tokens(n, seed=w.seed + 7)
     else:
-        n = min(w.n_kv, 131072)
-        nq = max(1, w.n_q * n // w.n_kv)
-        s = w.with_tokens(n, n_q=nq, seed=w.seed + 7)
-    s1 = dataclasses.replace(s, B=1, H=1)
-    inp = li.make_inputs(s1)
+        n = max(1024, min(w.n_kv, n_kv) // 1024 * 1024)
+        s = w.with_tokens(n, n_q=max(1, w.n_q * n // w.n_kv), seed=w.seed + 7)
+    return dataclasses.replace(s, B=1, H=1)
+
+
+def time_oracle(s: li.Workload) -> float:
+    from oracle import lact_oracle as O
+    inp = li.make_inputs(s)
     t0 = time.perf_counter()
-    O.run_workload(s1, inp, token_slice=65536)
-    dt = time.perf_counter() - t0
-    threads = blas_threads()
+    O.run_workload(s, inp, token_slice=65536)
+    return time.perf_counter() - t0
+
+
+def size_sample(w: li.Workload, seconds: float) -> li.Workload:
+    """A sample of the workload sized for about `seconds` of oracle time:
+    timed calibration runs from 16,384 update tokens, grown (at most 8x per
+    run, since small runs carry a fixed cost) until one takes over half the
+    target."""
+    s = oracle_sample(w, 16384)
+    while True:
+        dt = max(time_oracle(s), 1e-3)
+        if dt >= 0.5 * seconds or s.n_kv >= w.n_kv:
+            break
+        s = oracle_sample(w, int(s.n_kv * min(8.0, seconds / dt)))
+    return oracle_sample(w, int(s.n_kv * seconds / dt))
+
+
+def cpu_baseline(w: li.Workload, seconds: float = 15.0, sample: li.Workload | None = None):
+    """The oracle, as it stands, on a bounded sample of the workload (one
+    (b, h), sized for about `seconds` of CPU time)."""
+    s1 = sample or size_sample(w, seconds)
+    dt = time_oracle(s1)
     toks = tokens_per_step(s1)
-    return {"value": toks / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+    return {"value": toks / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
             "sample": f"1 (b,h) of the workload: {s1.n_kv} update + {s1.n_q if s1.order == 'set' else 0} "
                       f"query tokens, d={s1.d}, dh={s1.dh}, {s1.opt}, {s1.order}; fp64 numpy/OpenBLAS; "
                       f"{dt:.2f} s; value = sample tokens / time",
@@ -188,9 +213,12 @@ def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    # each step a sample sized so that the whole run takes about two minutes
+    per_step = min(20.0, max(2.0, 120.0 / max(1, args.warmup + args.steps)))
+    sample = size_sample(w, per_step)
     res = []
     for i in range(args.warmup + args.steps):
-        r = cpu_baseline(w)
+        r = cpu_baseline(w, sample=sample)
         if i >= args.warmup:
             res.append(r)
     val = statistics.median(r["value"] for r in res)
@@ -209,6 +237,9 @@ def run_reference(args, w):
 def main():
     args = parse()
     w = li.WORKLOADS[args.workload]
+    if args.update_tokens is not None or args.query_tokens is not None:
+        w = w.with_tokens(args.update_tokens or w.n_kv, n_q=args.query_tokens)
+        w = dataclasses.replace(w, name=f"{w.name} (reduced: {w.n_kv} update, {w.n_q} query tokens per head)")
     if args.impl == "reference":
         return run_reference(args, w)
     rank, world, local = dist_env()
