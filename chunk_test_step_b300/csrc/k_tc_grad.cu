@@ -65,7 +65,15 @@ constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s per wait
 
-enum { B_W = 0, B_KVF = 1, B_KVE = 1 + STAGES, B_FWDF = 1 + 2 * STAGES, B_FWDE, B_BF, B_BE, B_ACC, B_DRAIN, NBARS };
+// Barriers. K and V halves of a stage are filled and released separately: K
+// is free again once the dW1/dW3 GEMMs of its tile are done, V once the dW2
+// GEMMs are. The gradient operand buffer has a dh1|dh3 part and a u' part,
+// likewise written and released separately.
+enum {
+    B_W = 0,
+    B_KF = 1, B_VF = 1 + STAGES, B_KE = 1 + 2 * STAGES, B_VE = 1 + 3 * STAGES,
+    B_FWDF = 1 + 4 * STAGES, B_FWDE, B_DHF, B_UF, B_DHE, B_UE, B_ACC, B_DRAIN, NBARS
+};
 
 struct GradArgs {
     const float* eta;      // [BH, n_total]
@@ -80,11 +88,40 @@ struct GradArgs {
     int* status;
 };
 
-__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// Packed fp32 pairs (two lanes of work per instruction on sm_100 and later).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 f2_make(float lo, float hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f2 v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+    f2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float tanh_approx(float x) {
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ uint32_t pack_f2(f2 v) {
+    float lo, hi;
+    f2_split(v, lo, hi);
+    return pack_bf16(lo, hi);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -112,13 +149,17 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         abort_flag = 0;
         mbar_init(bar(B_W), 1);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar(B_KVF + s), 1);
-            mbar_init(bar(B_KVE + s), 1);
+            mbar_init(bar(B_KF + s), 1);
+            mbar_init(bar(B_VF + s), 1);
+            mbar_init(bar(B_KE + s), 1);
+            mbar_init(bar(B_VE + s), 1);
         }
         mbar_init(bar(B_FWDF), 1);
         mbar_init(bar(B_FWDE), 8);
-        mbar_init(bar(B_BF), 8);
-        mbar_init(bar(B_BE), 1);
+        mbar_init(bar(B_DHF), 8);
+        mbar_init(bar(B_UF), 8);
+        mbar_init(bar(B_DHE), 1);
+        mbar_init(bar(B_UE), 1);
         mbar_init(bar(B_ACC), 1);
         mbar_init(bar(B_DRAIN), 1);
         fence_mbar_init();
@@ -163,24 +204,30 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 tma_prefetch_l2_3d(&tm_v, 64, tok, bh);
             };
             for (int i = 0; i < PF; ++i) prefetch(i);
-            int issued = 0;
+            int issued_k = 0, issued_v = 0;
             for (int i = 0; i < count && !*abort_v; ++i) {
                 prefetch(i + PF);
                 const int s = i % STAGES;
-                if (i >= STAGES && !mbar_wait(bar(B_KVE + s), ((i / STAGES) - 1) & 1, WAIT_NS)) { give_up(); break; }
+                const uint32_t ph = ((i / STAGES) - 1) & 1;
                 const int tok = (int)(a.t0 + (int64_t)(tile_begin + i) * TT);
                 const uint32_t st = base + OFF_KV + s * KV_STAGE;
-                mbar_expect_tx(bar(B_KVF + s), 4 * BOX);
-                tma_load_3d(st + 0 * BOX, &tm_k, bar(B_KVF + s), 0, tok, bh);
-                tma_load_3d(st + 1 * BOX, &tm_k, bar(B_KVF + s), 64, tok, bh);
-                tma_load_3d(st + 2 * BOX, &tm_v, bar(B_KVF + s), 0, tok, bh);
-                tma_load_3d(st + 3 * BOX, &tm_v, bar(B_KVF + s), 64, tok, bh);
-                issued = i + 1;
+                if (i >= STAGES && !mbar_wait(bar(B_KE + s), ph, WAIT_NS)) { give_up(); break; }
+                mbar_expect_tx(bar(B_KF + s), 2 * BOX);
+                tma_load_3d(st + 0 * BOX, &tm_k, bar(B_KF + s), 0, tok, bh);
+                tma_load_3d(st + 1 * BOX, &tm_k, bar(B_KF + s), 64, tok, bh);
+                issued_k = i + 1;
+                if (i >= STAGES && !mbar_wait(bar(B_VE + s), ph, WAIT_NS)) { give_up(); break; }
+                mbar_expect_tx(bar(B_VF + s), 2 * BOX);
+                tma_load_3d(st + 2 * BOX, &tm_v, bar(B_VF + s), 0, tok, bh);
+                tma_load_3d(st + 3 * BOX, &tm_v, bar(B_VF + s), 64, tok, bh);
+                issued_v = i + 1;
             }
             // drain: the copies this thread started must land before the CTA exits
             mbar_wait(bar(B_W), 0, WAIT_NS);
-            for (int i = max(0, issued - STAGES); i < issued; ++i)
-                mbar_wait(bar(B_KVF + i % STAGES), (i / STAGES) & 1, WAIT_NS);
+            for (int i = max(0, issued_k - STAGES); i < issued_k; ++i)
+                mbar_wait(bar(B_KF + i % STAGES), (i / STAGES) & 1, WAIT_NS);
+            for (int i = max(0, issued_v - STAGES); i < issued_v; ++i)
+                mbar_wait(bar(B_VF + i % STAGES), (i / STAGES) & 1, WAIT_NS);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -203,18 +250,21 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             const uint32_t t_dw13 = tmem + COL_DW13, t_dw2 = tmem + COL_DW2;
             bool ok = mbar_wait(bar(B_W), 0, WAIT_NS);
             if (!ok) give_up();
-            auto issue_grad = [&](int i) {
-                const int s = i % STAGES;
-                const uint64_t so = (uint64_t)(s * KV_STAGE) >> 4;
-                const uint32_t first = i > 0 ? 1u : 0u;
+            auto issue_g13 = [&](int i) {
+                const uint64_t so = (uint64_t)((i % STAGES) * KV_STAGE) >> 4;
 #pragma unroll
-                for (int j = 0; j < TT / 16; ++j) {
-                    const uint32_t acc = j > 0 ? 1u : first;
-                    mma_bf16(t_dw13, dKT + so + j * 128, dDH + j * 128, i_g13, acc);
-                    mma_bf16(t_dw2, dKT + so + V_OFF + j * 128, dU + j * 128, i_g2, acc);
-                }
-                mma_commit(bar(B_KVE + s));
-                mma_commit(bar(B_BE));
+                for (int j = 0; j < TT / 16; ++j)
+                    mma_bf16(t_dw13, dKT + so + j * 128, dDH + j * 128, i_g13, (i > 0 || j > 0) ? 1u : 0u);
+                mma_commit(bar(B_KE + i % STAGES));
+                mma_commit(bar(B_DHE));
+            };
+            auto issue_g2 = [&](int i) {
+                const uint64_t so = (uint64_t)((i % STAGES) * KV_STAGE) >> 4;
+#pragma unroll
+                for (int j = 0; j < TT / 16; ++j)
+                    mma_bf16(t_dw2, dKT + so + V_OFF + j * 128, dU + j * 128, i_g2, (i > 0 || j > 0) ? 1u : 0u);
+                mma_commit(bar(B_VE + i % STAGES));
+                mma_commit(bar(B_UE));
             };
             auto issue_fwd = [&](int i) {
                 const uint64_t so = (uint64_t)((i % STAGES) * KV_STAGE) >> 4;
@@ -222,33 +272,44 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 for (int j = 0; j < D / 16; ++j) {
                     const uint64_t ko = (uint64_t)((j >> 2) * BOX + (j & 3) * 32) >> 4;
                     mma_bf16(t_h13, dK + so + ko, dWc + ko, i_fwd13, j > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    const uint64_t ko = (uint64_t)((j >> 2) * BOX + (j & 3) * 32) >> 4;
                     mma_bf16(t_a, dK + so + V_OFF + ko, dW2 + j * 128, i_fwda, j > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(B_FWDF));
             };
-            // Issue whichever is ready first: the gradient GEMMs of tile g (its
-            // dh1, dh3, u' are written) or the forward GEMMs of tile f (its K/V
-            // have landed and the epilogue has read tile f-1 out of TMEM). A
-            // gradient never queues behind a K/V load this way.
-            int f = 0, g = 0;
+            // Issue whichever is ready first: the dW1/dW3 GEMMs of tile g13
+            // (its dh1, dh3 are written), the dW2 GEMMs of tile g2 (its u' is
+            // written), or the forward GEMMs of tile f (its K/V have landed
+            // and the epilogue has read tile f-1 out of TMEM).
+            int f = 0, g13 = 0, g2 = 0;
             uint64_t deadline = globaltimer_ns() + WAIT_NS;
-            while (ok && g < count && !*abort_v) {
+            while (ok && g2 < count && !*abort_v) {
                 bool progress = false;
-                if (g < f && mbar_probe(bar(B_BF), g & 1)) {
+                if (g13 < f && mbar_probe(bar(B_DHF), g13 & 1)) {
                     tc_fence_after();
-                    issue_grad(g++);
+                    issue_g13(g13++);
                     progress = true;
-                } else if (f < count && (f == 0 || mbar_probe(bar(B_FWDE), (f - 1) & 1)) &&
-                           mbar_probe(bar(B_KVF + f % STAGES), (f / STAGES) & 1)) {
+                }
+                if (g2 < g13 && mbar_probe(bar(B_UF), g2 & 1)) {
+                    tc_fence_after();
+                    issue_g2(g2++);
+                    progress = true;
+                }
+                if (f < count && (f == 0 || mbar_probe(bar(B_FWDE), (f - 1) & 1)) &&
+                    mbar_probe(bar(B_KF + f % STAGES), (f / STAGES) & 1) &&
+                    mbar_probe(bar(B_VF + f % STAGES), (f / STAGES) & 1)) {
                     tc_fence_after();
                     issue_fwd(f++);
                     progress = true;
                 }
                 if (progress) {
                     deadline = globaltimer_ns() + WAIT_NS;
-                } else {
-                    __nanosleep(32);   // leave issue slots to the epilogue warps
-                    if (globaltimer_ns() > deadline) { give_up(); ok = false; }
+                } else if (globaltimer_ns() > deadline) {
+                    give_up();
+                    ok = false;
                 }
             }
             mma_commit(bar(B_ACC));
@@ -275,6 +336,7 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             return (i < count && tok < a.n) ? eta_h[tok] : 0.0f;
         };
         float e_next = eta_of(0), e_next2 = eta_of(1);
+        const f2 half2 = f2_make(0.5f, 0.5f), one2 = f2_make(1.0f, 1.0f), mone2 = f2_make(-1.0f, -1.0f);
         for (int i = 0; i < count; ++i) {
             const float e = e_next;
             e_next = e_next2;
@@ -292,39 +354,50 @@ k_grad_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_FWDE));
-            const float ne = -e;
+            // Per hidden unit (pairs of units per instruction):
+            //   s = sigmoid(h1) = 0.5 tanh(h1 / 2) + 0.5,  silu = h1 s
+            //   u'  = -eta silu h3                      (dW2 operand)
+            //   du  = -eta a                            (a = (W2^T v))
+            //   dh3 = du silu,  dh1 = du h3 (s + silu (1 - s))
+            const f2 ne2 = f2_make(-e, -e);
             uint32_t p1[16], p3[16], pu[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                float d1[2], d3[2], uu[2];
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const float x1 = __uint_as_float(h1[j + t]);
-                    const float x3 = __uint_as_float(h3[j + t]);
-                    const float s = sigmoid_fast(x1);
-                    const float si = x1 * s;                       // silu(h1)
-                    const float du = __uint_as_float(av[j + t]) * ne;
-                    uu[t] = si * x3 * ne;                          // -eta u
-                    d3[t] = du * si;                               // dL/dh3
-                    d1[t] = du * x3 * fmaf(-si, s, s + si);        // du h3 silu'(h1)
-                }
-                p1[j / 2] = pack_bf16(d1[0], d1[1]);
-                p3[j / 2] = pack_bf16(d3[0], d3[1]);
-                pu[j / 2] = pack_bf16(uu[0], uu[1]);
+                const f2 x1 = f2_make(__uint_as_float(h1[j]), __uint_as_float(h1[j + 1]));
+                const f2 x3 = f2_make(__uint_as_float(h3[j]), __uint_as_float(h3[j + 1]));
+                const f2 av2 = f2_make(__uint_as_float(av[j]), __uint_as_float(av[j + 1]));
+                float hx0, hx1;
+                f2_split(f2_mul(x1, half2), hx0, hx1);
+                const f2 t = f2_make(tanh_approx(hx0), tanh_approx(hx1));
+                const f2 sg = f2_fma(t, half2, half2);            // sigmoid(h1)
+                const f2 si = f2_mul(x1, sg);                     // silu(h1)
+                const f2 x3n = f2_mul(x3, ne2);                   // -eta h3
+                const f2 du = f2_mul(av2, ne2);                   // -eta a
+                const f2 oms = f2_fma(sg, mone2, one2);           // 1 - s
+                const f2 g = f2_fma(si, oms, sg);                 // silu'(h1)
+                pu[j / 2] = pack_f2(f2_mul(si, x3n));
+                p3[j / 2] = pack_f2(f2_mul(du, si));
+                p1[j / 2] = pack_f2(f2_mul(f2_mul(du, x3), g));
             }
-            if (i >= 1 && !mbar_wait_warp(bar(B_BE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
+            if (i >= 1 && !mbar_wait_warp(bar(B_DHE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t off = boff[c];
                 *reinterpret_cast<uint4*>(bbuf + off) = make_uint4(p1[4 * c], p1[4 * c + 1], p1[4 * c + 2], p1[4 * c + 3]);
                 *reinterpret_cast<uint4*>(bbuf + BOX + off) =
                     make_uint4(p3[4 * c], p3[4 * c + 1], p3[4 * c + 2], p3[4 * c + 3]);
-                *reinterpret_cast<uint4*>(bbuf + 2 * BOX + off) =
-                    make_uint4(pu[4 * c], pu[4 * c + 1], pu[4 * c + 2], pu[4 * c + 3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_BF));
+            if (lane == 0) mbar_arrive(bar(B_DHF));
+            if (i >= 1 && !mbar_wait_warp(bar(B_UE), (i - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(bbuf + 2 * BOX + boff[c]) =
+                    make_uint4(pu[4 * c], pu[4 * c + 1], pu[4 * c + 2], pu[4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_UF));
         }
         // ---- the CTA's partial dW out of TMEM
         if (ok && !*abort_v && mbar_wait_warp(bar(B_ACC), 0, WAIT_NS)) {
