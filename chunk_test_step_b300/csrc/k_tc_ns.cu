@@ -2,9 +2,9 @@
 // (LaCT review page, "Local attention and nonlinear memory work together":
 // Muon transforms each matrix gradient with Newton-Schulz iterations).
 //
-// One CTA per gradient matrix G (3 per head), for matrices whose short side is
-// 128 and long side n <= 512 (a multiple of 64). On the orientation with
-// rows <= cols (X is 128 x n):
+// One thread-block cluster per gradient matrix G (3 per head), for matrices
+// whose short side is 128 and long side n <= 512 (a multiple of 128). On the
+// orientation with rows <= cols (X is 128 x n):
 //   X = G / (||G||_F + 1e-7)
 //   repeat ns_steps times:
 //     A  = Xb Xb^T             Xb = bf16(X): K-major operand, both sides   (TMEM)
@@ -12,14 +12,22 @@
 //     B  = b A + c AA          fp32, from the unrounded A
 //     BX = Bb Xb               Bb = bf16(B) K-major; Xb read MN-major     (TMEM)
 //     X  = a X + BX            fp32
-// The bf16 copy Xb stays in shared memory for the whole iteration (it is the
-// operand of two GEMMs in two orientations); the fp32 X lives in an
-// L2-resident scratch row per thread. The result overwrites G in G's own
-// orientation.
+// The cluster has n/128 CTAs; CTA j owns columns [128 j, 128 j + 128) of X.
+// Every CTA holds the whole bf16 Xb in shared memory (the operand of A) and
+// forms A, AA and B itself (they are small: 128 x 128); it forms only its own
+// 128 columns of BX and keeps its fp32 columns of X in TMEM, so nothing of the
+// iteration leaves the chip. After each update a CTA writes its new bf16
+// columns (two 16 KB atoms, contiguous) into its own Xb and pushes them with
+// one bulk copy into the Xb of every other CTA of the cluster (distributed
+// shared memory), completing on that CTA's mbarrier. Two cluster-wide
+// handshakes per iteration order this: "every CTA's A GEMM has finished
+// reading Xb" before anyone overwrites it, and "every CTA's columns have
+// landed" before the next A GEMM.
 //
-// 256 threads: thread = row of X (TMEM lane) and half of its columns; thread
-// 0 also issues the MMAs. Every wait is bounded and its outcome made
-// block-uniform before any barrier that depends on it.
+// 256 threads: thread = row of X (TMEM lane) and half of the CTA's columns;
+// thread 0 also issues the MMAs. Every mbarrier wait is bounded and its
+// outcome made block-uniform; the hardware cluster barrier is used only at
+// entry and exit, which every CTA reaches unconditionally.
 #include "lact_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -31,18 +39,20 @@ using namespace tc;
 
 constexpr int M = 128;
 constexpr int NMAX = 512;
+constexpr int CB = 128;                            // columns of X per CTA
 constexpr int NTHREADS = 256;
 constexpr uint32_t ATOM = M * 128;                 // [128 rows][64 bf16] = 16 KB
 constexpr uint32_t OFF_X = 0;                      // n/64 atoms of Xb
 constexpr uint32_t OFF_A = (NMAX / 64) * ATOM;     // 2 atoms of Ab
 constexpr uint32_t OFF_B = OFF_A + 2 * ATOM;       // 2 atoms of Bb
-constexpr uint32_t SMEM_BYTES = OFF_B + 2 * ATOM + 1024;
-constexpr uint32_t COL_A = 0, COL_AA = 128, COL_BX = 0;
+constexpr int SROW = CB + 1;                       // fp32 staging row stride (words)
+constexpr uint32_t SMEM_STAGE = M * SROW * 4;      // staging of this CTA's fp32 columns, from OFF_A
+constexpr uint32_t SMEM_BYTES = (OFF_A + SMEM_STAGE > OFF_B + 2 * ATOM ? OFF_A + SMEM_STAGE : OFF_B + 2 * ATOM) + 1024;
+constexpr uint32_t COL_A = 0, COL_AA = 128, COL_BX = 256, COL_X = 384;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 struct NsArgs {
     float* g[3];      // gradients in place: W1 [BH,dh,d], W2 [BH,d,dh], W3 [BH,dh,d]
-    float* xs;        // fp32 X scratch [3*BH][M][n]
     int BH, d, dh, n, steps;
     float a, b, c;
     int* status;
@@ -65,68 +75,123 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
 __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t mbar;
+    __shared__ __align__(8) uint64_t mbar, sync_a, sync_x;
     __shared__ uint32_t tmem_slot;
     __shared__ float red[NTHREADS / 32];
-    __shared__ int failed;
+    __shared__ float norm_part[NMAX / CB];   // partial sums of squares, one per CTA of the cluster
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int mi = blockIdx.x, which = mi / a.BH, bh = mi % a.BH;
+    const int n = a.n;
+    const int cs = n / CB;                         // CTAs in the cluster
+    const uint32_t rank = cluster_rank();
+    const int mi = blockIdx.x / cs, which = mi / a.BH, bh = mi % a.BH;
     const int rows = which == 1 ? a.d : a.dh, cols = which == 1 ? a.dh : a.d;
     const bool tr = rows > cols;
-    const int n = a.n;
     float* G = a.g[which] + (size_t)bh * a.d * a.dh;
-    float* X = a.xs + (size_t)mi * M * n;
     const uint32_t base = smem_u32(sm);
     const uint32_t bar = smem_u32(&mbar);
+    const uint32_t bar_a = smem_u32(&sync_a), bar_x = smem_u32(&sync_x);
+    const int c0 = (int)rank * CB;                 // first column owned by this CTA
 
     if (tid == 0) {
-        failed = (*reinterpret_cast<volatile int*>(a.status) & ST_TIMEOUT) ? 1 : 0;
         mbar_init(bar, 1);
+        mbar_init(bar_a, cs);   // one arrive per CTA of the cluster
+        mbar_init(bar_x, 1);    // own arrive + the bytes of the other CTAs' columns
         fence_mbar_init();
     }
-    __syncthreads();
-    if (failed) return;
+    // barrier initialisation visible to the whole cluster before any remote arrive
+    cluster_sync_all();
     if (warp == 1) {
         __syncwarp();
         tmem_alloc(smem_u32(&tmem_slot), 512);
         tmem_relinquish();
     }
-    // ---- X = G / (||G||_F + eps), as fp32 rows and as the bf16 operand
-    float ss = 0.f;
-    for (int i = tid; i < rows * cols; i += NTHREADS) ss = fmaf(G[i], G[i], ss);
+    // ---- X = G / (||G||_F + eps). Each CTA reads only its own columns of X
+    // (a quarter of G for n = 512) into fp32 staging (rows padded to 129
+    // floats, so a warp's 32 rows fall in 32 banks), sums their squares, and
+    // posts the partial sum to every CTA of the cluster; every CTA adds the
+    // partials in rank order, so all hold the same norm.
+    const int q = warp & 3, half = warp >> 2;
+    const int row = 32 * q + lane;             // row of X owned by this thread
+    float* stage = reinterpret_cast<float*>(sm + OFF_A);   // [128 rows][SROW] fp32
+    const float4* G4 = reinterpret_cast<const float4*>(G);
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 16
+    for (int i = tid; i < M * CB / 4; i += NTHREADS) {
+        // four consecutive elements of G: X[gc + t][gr] when G is stored tall
+        // (its rows are columns of X), else X[gr][gc + t]
+        const int gr = tr ? c0 + (4 * i) / M : (4 * i) / CB;
+        const int gc = tr ? (4 * i) % M : c0 + (4 * i) % CB;
+        const float4 v = G4[((size_t)gr * cols + gc) / 4];
+        s4[i & 3] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, s4[i & 3]))));
+        const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int xr = tr ? gc + t : gr, xc = tr ? gr : gc + t;
+            stage[xr * SROW + (xc - c0)] = x[t];
+        }
+    }
+    float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) red[warp] = ss;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    float tot = 0.f;
-    for (int w = 0; w < NTHREADS / 32; ++w) tot += red[w];
-    const float nrm = sqrtf(tot) + 1e-7f;
-    const int q = warp & 3, half = warp >> 2;
-    const int row = 32 * q + lane;             // row of X owned by this thread
-    const int nh = n / 2;                      // its columns: [half * nh, half * nh + nh)
-    // Element (row, j) of X is G[row][j], or G[j][row] when G is stored tall:
-    // either way a warp's 32 rows read 32 consecutive or row-contiguous words.
-    for (int c0 = half * nh; c0 < half * nh + nh; c0 += 8) {
-        float x[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-            x[t] = (tr ? G[(size_t)(c0 + t) * cols + row] : G[(size_t)row * cols + c0 + t]) / nrm;
-        float* xr = X + (size_t)row * n + c0;
-        *reinterpret_cast<float4*>(xr) = make_float4(x[0], x[1], x[2], x[3]);
-        *reinterpret_cast<float4*>(xr + 4) = make_float4(x[4], x[5], x[6], x[7]);
-        *reinterpret_cast<uint4*>(sm + OFF_X + atom_off(row, c0)) = pack8(x);
+    const uint32_t tmem = tmem_slot;           // allocated by warp 1 before the barrier above
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+    if (tid == 0) {
+        float part = 0.f;
+        for (int w = 0; w < NTHREADS / 32; ++w) part += red[w];
+        for (int r = 0; r < cs; ++r) {
+            st_cluster_f32(mapa_shared(smem_u32(&norm_part[rank]), (uint32_t)r), part);
+            mbar_arrive_cluster(mapa_shared(bar_a, (uint32_t)r));
+        }
     }
+    bool ok = __syncthreads_and(mbar_wait_cluster(bar_a, 0, WAIT_NS) ? 1 : 0) != 0;
+    float tot = 0.f;
+    for (int r = 0; r < cs; ++r) tot += norm_part[r];
+    const float nrm = sqrtf(tot) + 1e-7f;
+    // this CTA's columns: fp32 into TMEM, bf16 into its block of Xb
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        float xv[32];
+        const int j0 = half * 64 + h * 32;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            xv[t] = stage[row * SROW + j0 + t] / nrm;
+            v[t] = __float_as_uint(xv[t]);
+        }
+        tmem_st32(lane_base + COL_X + j0, v);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(sm + OFF_X + atom_off(row, c0 + j0 + 8 * c)) = pack8(xv + 8 * c);
+    }
+    tmem_wait_st();
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_slot;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-    uint32_t phase = 0;
-    bool ok = true;
+    const uint32_t xblock = base + OFF_X + (uint32_t)(c0 / 64) * ATOM;   // this CTA's columns of Xb
+    constexpr uint32_t XBLOCK_BYTES = 2 * ATOM;
+    // Own columns of Xb out to the other CTAs, theirs in; the bytes are
+    // counted on bar_x. Phase 0 of bar_a and bar_x belong to the set-up, so
+    // iteration `it` uses phase it + 1.
+    auto exchange_columns = [&](uint32_t parity, bool send) -> bool {
+        if (tid == 0) {
+            mbar_expect_tx(bar_x, (uint32_t)(cs - 1) * XBLOCK_BYTES);
+            if (send)
+                for (int r = 0; r < cs; ++r)
+                    if (r != (int)rank)
+                        bulk_copy_to_cluster(mapa_shared(xblock, (uint32_t)r), xblock, XBLOCK_BYTES,
+                                             mapa_shared(bar_x, (uint32_t)r));
+        }
+        return __syncthreads_and(mbar_wait_cluster(bar_x, parity, WAIT_NS) ? 1 : 0) != 0;
+    };
+    if (!exchange_columns(0, ok)) ok = false;
+    tc_fence_after();
 
+    uint32_t phase = 0;
     // Wait for the MMAs just committed; the outcome is made block-uniform so
     // that every thread takes the same path through the barriers below.
     auto mma_done = [&]() -> bool {
@@ -142,131 +207,154 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         __syncthreads();
         tc_fence_after();
     };
-
+    // "My A GEMM is done with Xb": thread 0 (which saw the MMA complete)
+    // arrives on the barrier of every CTA of the cluster.
+    auto arrive_a_done = [&]() {
+        if (tid == 0)
+            for (int r = 0; r < cs; ++r) mbar_arrive_cluster(mapa_shared(bar_a, (uint32_t)r));
+    };
+    // Bounded wait on a local cluster barrier, made block-uniform.
+    auto cluster_wait = [&](uint32_t b, uint32_t parity) -> bool {
+        return __syncthreads_and(mbar_wait_cluster(b, parity, WAIT_NS) ? 1 : 0) != 0;
+    };
     const uint32_t i_xx = idesc_bf16_f32(M, M, 0, 0);
     const uint32_t i_aa = idesc_bf16_f32(M, M, 0, 1);
+    const uint32_t i_bx = idesc_bf16_f32(M, CB, 0, 1);
     const uint64_t dX = sdesc_sw128(base + OFF_X, 16, 1024);      // Xb K-major
     const uint64_t dXmn = sdesc_sw128(base + OFF_X, ATOM, 1024);  // Xb MN-major
     const uint64_t dA = sdesc_sw128(base + OFF_A, 16, 1024);      // Ab K-major
     const uint64_t dAmn = sdesc_sw128(base + OFF_A, ATOM, 1024);  // Ab MN-major
     const uint64_t dB = sdesc_sw128(base + OFF_B, 16, 1024);      // Bb K-major
-    for (int it = 0; it < a.steps && ok; ++it) {
+    for (int it = 0; it < a.steps; ++it) {
         // A = Xb Xb^T
-        if (tid == 0) {
+        if (ok && tid == 0) {
             for (int j = 0; j < n / 16; ++j) {
                 const uint64_t ko = (uint64_t)((j >> 2) * ATOM + (j & 3) * 32) >> 4;
                 mma_bf16(tmem + COL_A, dX + ko, dX + ko, i_xx, j > 0 ? 1u : 0u);
             }
             mma_commit(bar);
         }
-        if (!mma_done()) { ok = false; break; }
-        // Ab = bf16(A)
+        if (ok && !mma_done()) ok = false;
+        // this CTA's last read of the other CTAs' columns of Xb in the iteration is over
+        arrive_a_done();
+        if (ok) {
+            // Ab = bf16(A)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t v[32];
-            const int c0 = half * 64 + h * 32;
-            tmem_ld32(lane_base + COL_A + c0, v);
-            tmem_wait_ld();
-            tmem_pin(v);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v[32];
+                const int j0 = half * 64 + h * 32;
+                tmem_ld32(lane_base + COL_A + j0, v);
+                tmem_wait_ld();
+                tmem_pin(v);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float x[8];
+                for (int c = 0; c < 4; ++c) {
+                    float x[8];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) x[t] = __uint_as_float(v[8 * c + t]);
-                *reinterpret_cast<uint4*>(sm + OFF_A + atom_off(row, c0 + 8 * c)) = pack8(x);
+                    for (int t = 0; t < 8; ++t) x[t] = __uint_as_float(v[8 * c + t]);
+                    *reinterpret_cast<uint4*>(sm + OFF_A + atom_off(row, j0 + 8 * c)) = pack8(x);
+                }
             }
-        }
-        sync_smem();
-        // AA = Ab Ab
-        if (tid == 0) {
-#pragma unroll
-            for (int j = 0; j < M / 16; ++j) {
-                const uint64_t ko = (uint64_t)((j >> 2) * ATOM + (j & 3) * 32) >> 4;
-                mma_bf16(tmem + COL_AA, dA + ko, dAmn + j * 128, i_aa, j > 0 ? 1u : 0u);
-            }
-            mma_commit(bar);
-        }
-        if (!mma_done()) { ok = false; break; }
-        // Bb = bf16(b A + c AA)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t va[32], vaa[32];
-            const int c0 = half * 64 + h * 32;
-            tmem_ld32(lane_base + COL_A + c0, va);
-            tmem_ld32(lane_base + COL_AA + c0, vaa);
-            tmem_wait_ld();
-            tmem_pin(va);
-            tmem_pin(vaa);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float bv[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t)
-                    bv[t] = fmaf(a.c, __uint_as_float(vaa[8 * c + t]), a.b * __uint_as_float(va[8 * c + t]));
-                *reinterpret_cast<uint4*>(sm + OFF_B + atom_off(row, c0 + 8 * c)) = pack8(bv);
-            }
-        }
-        sync_smem();
-        // BX = Bb Xb (N in pieces of at most 256)
-        if (tid == 0) {
-            for (int nb = 0; nb < n; nb += 256) {
-                const int nn = n - nb < 256 ? n - nb : 256;
-                const uint32_t idx = idesc_bf16_f32(M, nn, 0, 1);
-                const uint64_t xo = (uint64_t)((nb / 64) * ATOM) >> 4;
+            sync_smem();
+            // AA = Ab Ab
+            if (tid == 0) {
 #pragma unroll
                 for (int j = 0; j < M / 16; ++j) {
                     const uint64_t ko = (uint64_t)((j >> 2) * ATOM + (j & 3) * 32) >> 4;
-                    mma_bf16(tmem + COL_BX + nb, dB + ko, dXmn + xo + j * 128, idx, j > 0 ? 1u : 0u);
+                    mma_bf16(tmem + COL_AA, dA + ko, dAmn + j * 128, i_aa, j > 0 ? 1u : 0u);
+                }
+                mma_commit(bar);
+            }
+            if (!mma_done()) ok = false;
+        }
+        if (ok) {
+            // Bb = bf16(b A + c AA)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t va[32], vaa[32];
+                const int j0 = half * 64 + h * 32;
+                tmem_ld32(lane_base + COL_A + j0, va);
+                tmem_ld32(lane_base + COL_AA + j0, vaa);
+                tmem_wait_ld();
+                tmem_pin(va);
+                tmem_pin(vaa);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float bv[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)
+                        bv[t] = fmaf(a.c, __uint_as_float(vaa[8 * c + t]), a.b * __uint_as_float(va[8 * c + t]));
+                    *reinterpret_cast<uint4*>(sm + OFF_B + atom_off(row, j0 + 8 * c)) = pack8(bv);
                 }
             }
-            mma_commit(bar);
-        }
-        if (!mma_done()) { ok = false; break; }
-        // X = a X + BX; Xb = bf16(X). The fp32 row chunk is fetched before the
-        // TMEM load so its L2 latency overlaps it.
-        for (int c0 = half * nh; c0 < half * nh + nh; c0 += 32) {
-            float* xr = X + (size_t)row * n + c0;
-            float4 x4[8];
+            sync_smem();
+            // BX_j = Bb Xb[:, c0 : c0 + 128]
+            if (tid == 0) {
+                const uint64_t xo = (uint64_t)((c0 / 64) * ATOM) >> 4;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) x4[t] = *reinterpret_cast<const float4*>(xr + 4 * t);
-            uint32_t v[32];
-            tmem_ld32(lane_base + COL_BX + c0, v);
-            tmem_wait_ld();
-            tmem_pin(v);
-            float xn[32];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                xn[4 * t + 0] = fmaf(a.a, x4[t].x, __uint_as_float(v[4 * t + 0]));
-                xn[4 * t + 1] = fmaf(a.a, x4[t].y, __uint_as_float(v[4 * t + 1]));
-                xn[4 * t + 2] = fmaf(a.a, x4[t].z, __uint_as_float(v[4 * t + 2]));
-                xn[4 * t + 3] = fmaf(a.a, x4[t].w, __uint_as_float(v[4 * t + 3]));
-                *reinterpret_cast<float4*>(xr + 4 * t) =
-                    make_float4(xn[4 * t], xn[4 * t + 1], xn[4 * t + 2], xn[4 * t + 3]);
+                for (int j = 0; j < M / 16; ++j) {
+                    const uint64_t ko = (uint64_t)((j >> 2) * ATOM + (j & 3) * 32) >> 4;
+                    mma_bf16(tmem + COL_BX, dB + ko, dXmn + xo + j * 128, i_bx, j > 0 ? 1u : 0u);
+                }
+                mma_commit(bar);
             }
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<uint4*>(sm + OFF_X + atom_off(row, c0 + 8 * c)) = pack8(xn + 8 * c);
+            if (!mma_done()) ok = false;
         }
-        sync_smem();
+        // no CTA still reads Xb with its A GEMM
+        if (!cluster_wait(bar_a, (it + 1) & 1)) ok = false;
+        if (ok) {
+            // X_j = a X_j + BX_j in TMEM; bf16(X_j) into Xb of every CTA
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j0 = half * 64 + h * 32;
+                uint32_t vx[32], vb[32];
+                tmem_ld32(lane_base + COL_X + j0, vx);
+                tmem_ld32(lane_base + COL_BX + j0, vb);
+                tmem_wait_ld();
+                tmem_pin(vx);
+                tmem_pin(vb);
+                float xn[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    xn[t] = fmaf(a.a, __uint_as_float(vx[t]), __uint_as_float(vb[t]));
+                    vx[t] = __float_as_uint(xn[t]);
+                }
+                tmem_st32(lane_base + COL_X + j0, vx);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4*>(sm + OFF_X + atom_off(row, c0 + j0 + 8 * c)) = pack8(xn + 8 * c);
+            }
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (!exchange_columns((it + 1) & 1, ok)) ok = false;
+        tc_fence_after();
     }
     if (!ok) {
-        if (lane == 0) atomicOr(a.status, ST_TIMEOUT);
+        if (tid == 0) atomicOr(a.status, ST_TIMEOUT);
     } else {
-        // result back into G's own orientation (this thread's row, as read)
-        for (int c0 = half * nh; c0 < half * nh + nh; c0 += 4) {
-            const float4 x4 = *reinterpret_cast<const float4*>(X + (size_t)row * n + c0);
+        // this CTA's columns back into G's own orientation
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j0 = half * 64 + h * 32;
+            uint32_t v[32];
+            tmem_ld32(lane_base + COL_X + j0, v);
+            tmem_wait_ld();
+            tmem_pin(v);
             if (tr) {
-                G[(size_t)(c0 + 0) * cols + row] = x4.x;
-                G[(size_t)(c0 + 1) * cols + row] = x4.y;
-                G[(size_t)(c0 + 2) * cols + row] = x4.z;
-                G[(size_t)(c0 + 3) * cols + row] = x4.w;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) G[(size_t)(c0 + j0 + t) * cols + row] = __uint_as_float(v[t]);
             } else {
-                *reinterpret_cast<float4*>(G + (size_t)row * cols + c0) = x4;
+                float* gr = G + (size_t)row * cols + c0 + j0;
+#pragma unroll
+                for (int t = 0; t < 32; t += 4)
+                    *reinterpret_cast<float4*>(gr + t) = make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]),
+                                                                    __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3]));
             }
         }
     }
-    // every MMA has completed once this commit lands (bounded drain), then
-    // TMEM is freed
+    // every MMA has completed once this commit lands (bounded drain)
     if (tid == 0) {
         mma_commit(bar);
         mbar_wait(bar, phase & 1, WAIT_NS);
@@ -278,6 +366,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // no CTA leaves while another may still write into its shared memory
+    cluster_sync_all();
 }
 
 }  // namespace
@@ -285,13 +375,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
 bool ns_tc_supported(const lact_state* st) {
     const int m = st->cfg.d < st->cfg.dh ? st->cfg.d : st->cfg.dh;
     const int n = st->cfg.d < st->cfg.dh ? st->cfg.dh : st->cfg.d;
-    return st->cfg.io_dtype == LACT_BF16 && m == M && n <= NMAX && n % 64 == 0;
+    return st->cfg.io_dtype == LACT_BF16 && m == M && n <= NMAX && n % CB == 0;
 }
 
 cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s) {
     NsArgs a;
     for (int m = 0; m < 3; ++m) a.g[m] = static_cast<float*>(g[m]);
-    a.xs = static_cast<float*>(st->ns[0]);
     a.BH = st->BH;
     a.d = st->cfg.d;
     a.dh = st->cfg.dh;
@@ -303,10 +392,23 @@ cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s)
     a.status = st->status;
     cudaError_t e = cudaFuncSetAttribute(k_ns_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    k_ns_tc<<<3 * st->BH, NTHREADS, SMEM_BYTES, s>>>(a);
+    const int cs = a.n / CB;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)(cs * 3 * st->BH));
+    lc.blockDim = dim3(NTHREADS);
+    lc.dynamicSmemBytes = SMEM_BYTES;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)cs;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&lc, k_ns_tc, a);
     g_launches++;
     g_tc_launches++;
-    return cudaGetLastError();
+    return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace lact
