@@ -30,6 +30,11 @@ static bool config_ok(const lact_config* c) {
     return true;
 }
 
+int64_t slice_cap(const lact_config& c) {
+    if (c.io_dtype != LACT_BF16 || c.d != 256) return 0;
+    return c.max_chunk < kSliceCap ? c.max_chunk : kSliceCap;
+}
+
 // Internal real type: fp64 for fp32 io, fp32 for bf16 io.
 static size_t real_size(const lact_config& c) { return c.io_dtype == LACT_F32 ? 8 : 4; }
 
@@ -50,6 +55,7 @@ WsLayout ws_layout(const lact_config& c) {
     L.ns[1] = take(3 * BH * mm * nn * rs);
     L.ns[2] = take(3 * BH * mm * mm * rs);
     L.ns[3] = take(3 * BH * mm * mm * rs);
+    L.inter = take((size_t)3 * BH * slice_cap(c) * c.dh * 2);
     L.status = take(64 * 4);
     L.total = off;
     return L;
@@ -129,6 +135,19 @@ static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* et
         }
         return LACT_OK;
     }
+    if (fwdbwd_tc_supported(st) && st->slice_cap > 0) {
+        // two kernels per token slice; the GEMMs write (or add to) out[] directly
+        PhaseTimer t(st, LACT_PHASE_GRAD, s);
+        cudaError_t e = cudaSuccess;
+        for (int64_t o = 0; o < k.n && e == cudaSuccess; o += st->slice_cap) {
+            const int64_t n = k.n - o < st->slice_cap ? k.n - o : st->slice_cap;
+            const TokView ks{k.p, k.n_total, k.t0 + o, n}, vs{v.p, v.n_total, v.t0 + o, n};
+            e = launch_fwdbwd_tc(st, ks, vs, eta, st->inter, st->slice_cap, s);
+            if (e == cudaSuccess) e = launch_wgrad_tc(st, ks, vs, st->inter, st->slice_cap, accumulate || o > 0, out, s);
+        }
+        t.done();
+        return cuda_status(e);
+    }
     int slots = 0;
     {
         PhaseTimer t(st, LACT_PHASE_GRAD, s);
@@ -196,6 +215,8 @@ lact_status lact_init_state(lact_state** out, const lact_config* cfg, void* d_ws
     }
     st->partial = st->ws + L.partial;
     for (int i = 0; i < 4; ++i) st->ns[i] = st->ws + L.ns[i];
+    st->inter = reinterpret_cast<bf16*>(st->ws + L.inter);
+    st->slice_cap = slice_cap(*cfg);
     st->status = reinterpret_cast<int*>(st->ws + L.status);
     st->last_stream = s;
     st->profiling = false;

@@ -26,11 +26,16 @@ struct WsLayout {
     size_t dW[3];      // real chunk gradients (Muon: overwritten by NS output), same layouts
     size_t partial;    // real split-K partials [kMaxSlots][3][BH][dh*d]
     size_t ns[4];      // real Newton-Schulz scratch: X, X', A, B over 3*BH matrices
+    size_t inter;      // bf16 per-token dh1, dh3, u' of one token slice [3][BH][slice_cap][dh] (two-kernel gradient)
     size_t status;     // int32[64]: [0] sticky status bits, [1..] diagnostics
     size_t total;
 };
 
 constexpr int kMaxSlots = 64;   // split-K partial slots
+constexpr int64_t kSliceCap = 4096;   // tokens per slice of the two-kernel gradient (its intermediates stay in L2)
+
+// Tokens per slice of the two-kernel gradient for this configuration (0 if unused).
+int64_t slice_cap(const lact_config& c);
 
 WsLayout ws_layout(const lact_config& c);
 
@@ -51,6 +56,8 @@ struct lact_state {
     void* dW[3];
     void* partial;
     void* ns[4];
+    lact::bf16* inter;
+    int64_t slice_cap;
     int* status;
     cudaStream_t last_stream;
     bool profiling;
@@ -126,6 +133,13 @@ bool ns_tc_supported(const lact_state* st);
 cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s);
 bool apply_tc_supported(const lact_state* st);
 cudaError_t launch_apply_tc(const lact_state* st, TokView q, void* o, cudaStream_t s);
+// Two-kernel chunk gradient (bf16 io, head dim 256): per-token dh1, dh3, u'
+// of a token slice, then the three weight-gradient GEMMs over the slice.
+bool fwdbwd_tc_supported(const lact_state* st);
+cudaError_t launch_fwdbwd_tc(const lact_state* st, TokView k, TokView v, const float* eta, bf16* inter,
+                             int64_t slice_cap, cudaStream_t s);
+cudaError_t launch_wgrad_tc(const lact_state* st, TokView k, TokView v, const bf16* inter, int64_t slice_cap,
+                            bool accumulate, void* const out[3], cudaStream_t s);
 cudaError_t launch_reduce(const lact_state* st, int slots, bool accumulate, void* const out[3],
                           cudaStream_t s);
 cudaError_t launch_newton_schulz(const lact_state* st, void* const g[3], cudaStream_t s);

@@ -67,12 +67,10 @@ def test_apply_matches_oracle(num, n_q):
 
 
 # ---------------------------------------------------- rows a2-a4: gradient
-@pytest.mark.parametrize("num,n", [(1, 1000 + 37), (2, 2048 + 5), (4, 4096 + 99), (5, 3 * 128 + 1),
-                                   (4, 1), (4, 127), (5, 128), (5, 37 * 128 + 5)])
-def test_chunk_gradient_matches_oracle(num, n):
+def _check_gradient(w):
     torch = _torch()
     from chunk_test_step_b300 import lact as L
-    w = li.WORKLOADS[num].with_tokens(n, seed=li.WORKLOADS[num].seed + 2000)
+    n = w.n_kv
     inp = li.make_inputs(w)
     layer = _layer(w, inp, max_chunk=n)
     k, v, e = to_device(inp.k), to_device(inp.v), to_device(inp.eta)
@@ -87,6 +85,19 @@ def test_chunk_gradient_matches_oracle(num, n):
             for m in range(3):
                 err = rel_l2(got[m][b, h], want[m])
                 assert err < TOL[w.dtype], (m, b, h, err)
+
+
+@pytest.mark.parametrize("num,n", [(1, 1000 + 37), (2, 2048 + 5), (4, 4096 + 99), (5, 3 * 128 + 1),
+                                   (4, 1), (4, 127), (5, 128), (5, 37 * 128 + 5), (2, 1), (2, 129)])
+def test_chunk_gradient_matches_oracle(num, n):
+    _check_gradient(li.WORKLOADS[num].with_tokens(n, seed=li.WORKLOADS[num].seed + 2000))
+
+
+def test_gradient_at_head_dim_256_spans_several_token_slices():
+    # head dim 256 takes the gradient per 4,096-token slice (two kernels per
+    # slice, the GEMMs adding into the result): three slices, the last ragged
+    w = dataclasses.replace(li.WORKLOADS[2], H=1)
+    _check_gradient(w.with_tokens(2 * 4096 + 77, seed=w.seed + 2100))
 
 
 # ------------------------------------------- rows a5-a7: optimiser + renorm
@@ -226,3 +237,21 @@ def test_profiling_counts_phases():
     assert all(prof[p]["calls"] == 1 for p in ("apply", "grad", "reduce", "ns", "update"))
     assert sum(prof[p]["launches"] for p in prof) == n1 - n0
     assert all(prof[p]["ms"] > 0 for p in prof)
+
+
+@pytest.mark.parametrize("num", [2, 4, 5])
+def test_bf16_workloads_run_on_tensor_core_kernels(num):
+    # every launch of the readout and gradient phases of the bf16 layers is a
+    # tcgen05 kernel (no CUDA-core stand-in)
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = _small(num)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    q, k, v, e = (to_device(x) for x in (inp.q, inp.k, inp.v, inp.eta))
+    L.lact_set_profiling(layer.handle, True)
+    order = L.LACT_CAUSAL_APPLY_THEN_UPDATE if w.order == "causal" else L.LACT_SET_UPDATE_THEN_APPLY
+    layer.sequence(order, q, k, v, e, w.chunk)
+    prof = L.lact_get_profile(layer.handle)
+    for ph in ("apply", "grad"):
+        assert prof[ph]["launches"] > 0 and prof[ph]["tensor_launches"] == prof[ph]["launches"], (ph, prof[ph])
