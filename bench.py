@@ -78,6 +78,26 @@ def tokens_per_step(w: li.Workload) -> int:
     return w.B * per
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one
+# full-size launch of the fused gradient kernel on the million-token layer,
+# from a one-pass ncu capture (summary: profiles/k_grad_tc_million_token_set.md).
+# It describes the kernel source it was taken on, identified by its hash.
+GRAD_TRAFFIC = {"workload": 5, "bytes": 4.45e9 + 221.58e6, "kernel_source": "k_tc_grad.cu",
+                "sha256_prefix": "6398275f0271f6a2"}
+
+
+def measured_traffic(w: li.Workload, reduced: bool):
+    import hashlib
+    if reduced or w.number != GRAD_TRAFFIC["workload"]:
+        return None
+    path = os.path.join(ROOT, "chunk_test_step_b300", "csrc", GRAD_TRAFFIC["kernel_source"])
+    try:
+        sha = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return GRAD_TRAFFIC["bytes"] if sha.startswith(GRAD_TRAFFIC["sha256_prefix"]) else None
+
+
 def peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
@@ -237,7 +257,8 @@ def run_reference(args, w):
 def main():
     args = parse()
     w = li.WORKLOADS[args.workload]
-    if args.update_tokens is not None or args.query_tokens is not None:
+    reduced = args.update_tokens is not None or args.query_tokens is not None
+    if reduced:
         w = w.with_tokens(args.update_tokens or w.n_kv, n_q=args.query_tokens)
         w = dataclasses.replace(w, name=f"{w.name} (reduced: {w.n_kv} update, {w.n_q} query tokens per head)")
     if args.impl == "reference":
@@ -334,23 +355,29 @@ def main():
     if st != L.LACT_OK:
         raise RuntimeError(f"device status after the timed region: {L.lact_status_str(st)}")
 
-    # ---- roofline of the dominant kernel (the fused gradient kernel)
+    # ---- roofline of the dominant phase: the chunk gradient (the fused
+    # kernel at head dim 128; two kernels per token slice at head dim 256),
+    # timed per call with CUDA events on the launching stream
     pk, pk_src = peaks()
     fl = flops(w)
     grad = prof["grad"]
-    grad_ms = grad["ms"] / max(1, grad["launches"])
-    grad_flop = fl["update"] / (1 if w.order == "set" else -(-w.n_kv // w.chunk))
+    chunks = 1 if w.order == "set" else -(-w.n_kv // w.chunk)
+    grad_ms = grad["ms"] / max(1, grad["calls"])
+    grad_flop = fl["update"] / chunks
     achieved = grad_flop / (grad_ms / 1e3) / 1e12
     tensor = grad["tensor_launches"] > 0
     if tensor:
         peak, bound, note = pk["bf16_tflops"], "tensor", f"dense bf16 burst, {pk_src}"
+        kernel = "k_grad_tc" if w.d == 128 else "k_fwdbwd_tc + k_wgrad_tc"
     else:
         # CUDA-core fp32 FMA: 148 SMs x 128 FMA/clk x 2 FLOP x max SM clock
         peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
         bound, note = "alu", "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"
+        kernel = "k_grad_simt"
     roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": None, "kernel": "grad", "peak_source": note,
-            "ms_per_launch": grad_ms, "flop_per_launch": grad_flop}
+            "traffic": measured_traffic(w, reduced), "traffic_unit": "bytes per launch", "kernel": kernel,
+            "peak_source": note, "ms_per_launch": grad_ms, "flop_per_launch": grad_flop,
+            "launches_per_call": grad["launches"] / max(1, grad["calls"])}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
