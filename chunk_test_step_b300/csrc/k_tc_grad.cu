@@ -474,15 +474,24 @@ cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const flo
 
     const int ntiles = (int)((k.n + TT - 1) / TT);
     const int units = BH * (dh / HB);
-    // One CTA per SM. Token splits: at most kMaxSlots, at least 16 tiles per
-    // CTA, and, where possible, a CTA count that fills whole waves.
-    int splits = ntiles / 16;
-    if (splits > kMaxSlots) splits = kMaxSlots;
-    if (splits < 1) splits = 1;
-    for (int sp = splits; sp >= 1; --sp)
-        if (((int64_t)units * sp) % st->num_sms == 0) { splits = sp; break; }
+    // Token splits (one CTA per SM; each split writes one fp32 partial per
+    // unit that the reduction reads back). Cost in units of one tile's time:
+    // waves x (tiles per CTA + ~3 tiles of pipeline fill and drain per CTA)
+    // + ~0.5 per split for writing and re-reading its partial sums. This picks
+    // one long wave where the grid allows (e.g. 48 units x 3 splits on 148
+    // SMs) and whole waves of shorter CTAs otherwise.
+    int splits = 1;
+    double best = 1e30;
+    for (int sp = 1; sp <= kMaxSlots && sp <= ntiles; ++sp) {
+        const int tps = (ntiles + sp - 1) / sp;
+        const int used = (ntiles + tps - 1) / tps;
+        if (used != sp) continue;
+        const int64_t ctas = (int64_t)units * sp;
+        const int64_t waves = (ctas + st->num_sms - 1) / st->num_sms;
+        const double cost = (double)waves * (tps + 3.0) + 0.5 * sp;
+        if (cost < best - 1e-9) { best = cost; splits = sp; }
+    }
     const int tps = (ntiles + splits - 1) / splits;
-    splits = (ntiles + tps - 1) / tps;
 
     GradArgs ga;
     ga.eta = eta;
