@@ -59,6 +59,21 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x: float, pg, device) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job rate: every rank processes its own units (weak scaling)."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def flops(w: li.Workload) -> dict:
     """Algorithmic FLOP of one layer call (per the method, no recompute)."""
     BH, d, dh = w.B * w.H, w.d, w.dh
@@ -321,14 +336,10 @@ def main():
     prof = L.lact_get_profile(layer.handle)
     L.lact_set_profiling(layer.handle, False)
     ck = clocks.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    if pg:
-        t = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
     ms_step = ms_total / args.steps
     tok = tokens_per_step(w)
-    value = tok * world / (ms_step / 1e3)
+    value = job_throughput(tok, world, ms_step)
 
     # ---- e2e: host (pinned) inputs copied in, the call, the output copied out
     ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
@@ -346,11 +357,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, pg, dev)
     st = L.lact_sync_status(layer.handle)
     if st != L.LACT_OK:
         raise RuntimeError(f"device status after the timed region: {L.lact_status_str(st)}")
@@ -388,7 +395,7 @@ def main():
                        "l2": "inputs larger than L2 (no flush)",
                        "tflops_per_s": fl["total"] / (ms_step / 1e3) / 1e12 * world},
             "roofline": roof,
-            "e2e": {"value": tok * world / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_throughput(tok, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches,
             "clocks": ck,
