@@ -10,10 +10,11 @@
 //   [H1 | H3] (TMEM, double-buffered) = Q . [W1_r ; W3_r]^T   (A, B K-major)
 //   U_r = silu(H1) * H3 -> bf16, swizzled K-major operand       (epilogue)
 //   O (TMEM, D cols) += U_r . W2[:, r]^T                        (A, B K-major)
-// so the MMA of block r+1 overlaps the epilogue of block r. At D = 128 the W
-// blocks are double-buffered through TMA; at D = 256 a W block is 96 KB and
-// single-buffered, and the blocks run one after another. At the end O leaves
-// TMEM as bf16.
+// so the MMA of block r+1 overlaps the epilogue of block r. The weights
+// stream through two TMA rings: [W1_r ; W3_r] in 64-wide head-dim pieces
+// (128 rows, 16 KB; 4 slots) and W2[:, r] (D rows x 64, 2 slots), so the
+// next block's weights load while the current block computes. At the end O
+// leaves TMEM as bf16.
 //
 // Warp roles (320 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer,
 // warps 2..9 epilogue (thread = query, 32 of the 64 hidden units). Every
@@ -30,17 +31,18 @@ using namespace tc;
 constexpr int HB = 64;
 constexpr int TT = 128;
 constexpr int NTHREADS = 320;
+constexpr int CSLOTS = 4;                           // [W1_r ; W3_r] piece ring
 constexpr uint32_t BOX = TT * 128;                  // [128 rows][64 bf16], 16 KB
 
-// Shared-memory layout for head dim D with `WS` W-block stages.
-template <int D, int WS>
+// Shared-memory layout for head dim D.
+template <int D>
 struct ApplyLayout {
-    static constexpr uint32_t OFF_Q = 0;                                  // D/64 k-atoms of the query tile
-    static constexpr uint32_t OFF_W = (D / 64) * BOX;                     // stage s: Wcat (D/64 atoms), W2 (D rows)
-    static constexpr uint32_t WC_BYTES = (D / 64) * BOX;
-    static constexpr uint32_t W2_BYTES = D * 128;
-    static constexpr uint32_t W_STAGE = WC_BYTES + W2_BYTES;
-    static constexpr uint32_t OFF_U = OFF_W + WS * W_STAGE;               // 2 buffers of [128 tok][64 hid]
+    static constexpr int NQ = D / 64;                                     // head-dim pieces
+    static constexpr uint32_t OFF_Q = 0;                                  // NQ k-atoms of the query tile
+    static constexpr uint32_t OFF_C = NQ * BOX;                           // CSLOTS pieces of [W1_r ; W3_r]
+    static constexpr uint32_t W2_BYTES = D * 128;                         // [D rows][64 hidden]
+    static constexpr uint32_t OFF_W2 = OFF_C + CSLOTS * BOX;              // 2 slots
+    static constexpr uint32_t OFF_U = OFF_W2 + 2 * W2_BYTES;              // 2 buffers of [128 tok][64 hid]
     static constexpr uint32_t SMEM_BYTES = OFF_U + 2 * BOX + 1024;
 };
 
@@ -49,7 +51,10 @@ constexpr uint32_t COL_O = 256;     // D columns
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-enum { B_Q = 0, B_WF = 1, B_WE = 3, B_HF = 5, B_HE = 7, B_UF = 9, B_UE = 11, B_O = 13, B_DRAIN = 14, NBARS = 15 };
+enum {
+    B_Q = 0, B_CF = 1, B_CE = 1 + CSLOTS, B_2F = 1 + 2 * CSLOTS, B_2E = B_2F + 2, B_HF = B_2E + 2, B_HE = B_HF + 2,
+    B_UF = B_HE + 2, B_UE = B_UF + 2, B_O = B_UE + 2, B_DRAIN, NBARS
+};
 
 struct ApplyArgs {
     bf16* o;             // [BH, n_total, D], same layout as q
@@ -66,10 +71,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&p);
 }
 
-template <int D, int WS>
+__device__ __forceinline__ float tanh_approx(float x) {
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w1,
            const __grid_constant__ CUtensorMap tm_w3, const __grid_constant__ CUtensorMap tm_w2, const ApplyArgs a) {
+    typedef ApplyLayout<D> Lo;
+    constexpr int NQ = Lo::NQ;
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[NBARS];
@@ -82,16 +95,18 @@ k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int R = a.dh / HB;
     const uint32_t base = smem_u32(sm);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
-    typedef ApplyLayout<D, WS> Lo;
-    constexpr uint32_t OFF_Q = Lo::OFF_Q, OFF_W = Lo::OFF_W, OFF_U = Lo::OFF_U, W_STAGE = Lo::W_STAGE;
 
     if (tid == 0) {
         skip_cta = (*reinterpret_cast<volatile int*>(a.status) & ST_TIMEOUT) ? 1 : 0;
         abort_flag = 0;
         mbar_init(bar(B_Q), 1);
+        for (int s = 0; s < CSLOTS; ++s) {
+            mbar_init(bar(B_CF + s), 1);
+            mbar_init(bar(B_CE + s), 1);
+        }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_WF + s), 1);
-            mbar_init(bar(B_WE + s), 1);
+            mbar_init(bar(B_2F + s), 1);
+            mbar_init(bar(B_2E + s), 1);
             mbar_init(bar(B_HF + s), 1);
             mbar_init(bar(B_HE + s), 8);
             mbar_init(bar(B_UF + s), 8);
@@ -121,69 +136,82 @@ k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     if (warp == 0) {
         if (lane == 0) {
             const int tok = (int)(a.t0 + (int64_t)tile * TT);
-            mbar_expect_tx(bar(B_Q), (D / 64) * BOX);
-            for (int at = 0; at < D / 64; ++at) tma_load_3d(base + OFF_Q + at * BOX, &tm_q, bar(B_Q), at * 64, tok, bh);
-            int issued = 0;
-            for (int r = 0; r < R && !*abort_v; ++r) {
-                const int s = r % WS;
-                if (r >= WS && !mbar_wait(bar(B_WE + s), ((r / WS) - 1) & 1, WAIT_NS)) { give_up(); break; }
-                const uint32_t st = base + OFF_W + s * W_STAGE;
+            mbar_expect_tx(bar(B_Q), NQ * BOX);
+            for (int qd = 0; qd < NQ; ++qd) tma_load_3d(base + Lo::OFF_Q + qd * BOX, &tm_q, bar(B_Q), qd * 64, tok, bh);
+            int issued_c = 0, issued_2 = 0;
+            bool ok = true;
+            for (int r = 0; r < R && ok && !*abort_v; ++r) {
                 const int wrow = bh * a.dh + r * HB;
-                mbar_expect_tx(bar(B_WF + s), W_STAGE);
-                for (int at = 0; at < D / 64; ++at) {
-                    tma_load_2d(st + at * BOX, &tm_w1, bar(B_WF + s), at * 64, wrow);
-                    tma_load_2d(st + at * BOX + BOX / 2, &tm_w3, bar(B_WF + s), at * 64, wrow);
+                for (int qd = 0; qd < NQ; ++qd) {
+                    const int i = r * NQ + qd, s = i % CSLOTS;
+                    if (i >= CSLOTS && !mbar_wait(bar(B_CE + s), ((i / CSLOTS) - 1) & 1, WAIT_NS)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = base + Lo::OFF_C + s * BOX;
+                    mbar_expect_tx(bar(B_CF + s), BOX);
+                    tma_load_2d(st, &tm_w1, bar(B_CF + s), qd * 64, wrow);
+                    tma_load_2d(st + BOX / 2, &tm_w3, bar(B_CF + s), qd * 64, wrow);
+                    issued_c = i + 1;
                 }
-                tma_load_2d(st + Lo::WC_BYTES, &tm_w2, bar(B_WF + s), r * HB, bh * D);
-                issued = r + 1;
+                if (!ok) break;
+                const int s2 = r & 1;
+                if (r >= 2 && !mbar_wait(bar(B_2E + s2), ((r >> 1) - 1) & 1, WAIT_NS)) { give_up(); break; }
+                mbar_expect_tx(bar(B_2F + s2), Lo::W2_BYTES);
+                tma_load_2d(base + Lo::OFF_W2 + s2 * Lo::W2_BYTES, &tm_w2, bar(B_2F + s2), r * HB, bh * D);
+                issued_2 = r + 1;
             }
+            // drain: the copies this thread started must land before the CTA exits
             mbar_wait(bar(B_Q), 0, WAIT_NS);
-            for (int r = (issued > WS ? issued - WS : 0); r < issued; ++r)
-                mbar_wait(bar(B_WF + (r % WS)), (r / WS) & 1, WAIT_NS);
+            for (int i = max(0, issued_c - CSLOTS); i < issued_c; ++i)
+                mbar_wait(bar(B_CF + i % CSLOTS), (i / CSLOTS) & 1, WAIT_NS);
+            for (int r = max(0, issued_2 - 2); r < issued_2; ++r) mbar_wait(bar(B_2F + (r & 1)), (r >> 1) & 1, WAIT_NS);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t i_h = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t i_o = idesc_bf16_f32(128, D, 0, 0);
             // descriptor bases; offsets (address / 16) are added as constants
-            const uint64_t dQ = sdesc_sw128(base + OFF_Q, 16, 1024);
-            const uint64_t dWc = sdesc_sw128(base + OFF_W, 16, 1024);
-            const uint64_t dW2 = sdesc_sw128(base + OFF_W + Lo::WC_BYTES, 16, 1024);
-            const uint64_t dU = sdesc_sw128(base + OFF_U, 16, 1024);
+            const uint64_t dQ = sdesc_sw128(base + Lo::OFF_Q, 16, 1024);
+            const uint64_t dC = sdesc_sw128(base + Lo::OFF_C, 16, 1024);
+            const uint64_t dW2 = sdesc_sw128(base + Lo::OFF_W2, 16, 1024);
+            const uint64_t dU = sdesc_sw128(base + Lo::OFF_U, 16, 1024);
             bool ok = mbar_wait(bar(B_Q), 0, WAIT_NS);
             if (!ok) give_up();
             auto out_mma = [&](int r) -> bool {
                 const int u = r & 1;
                 if (!mbar_wait(bar(B_UF + u), (r >> 1) & 1, WAIT_NS)) return false;
+                if (!mbar_wait(bar(B_2F + u), (r >> 1) & 1, WAIT_NS)) return false;
                 tc_fence_after();
-                const uint64_t wo = (uint64_t)((r % WS) * W_STAGE) >> 4, uo = (uint64_t)(u * BOX) >> 4;
+                const uint64_t wo = (uint64_t)(u * Lo::W2_BYTES) >> 4, uo = (uint64_t)(u * BOX) >> 4;
                 const uint32_t first = r > 0 ? 1u : 0u;
 #pragma unroll
                 for (int j = 0; j < HB / 16; ++j)
                     mma_bf16(tmem + COL_O, dU + uo + j * 2, dW2 + wo + j * 2, i_o, j > 0 ? 1u : first);
-                mma_commit(bar(B_WE + r % WS));
+                mma_commit(bar(B_2E + u));
                 mma_commit(bar(B_UE + u));
                 return true;
             };
             for (int r = 0; r < R && ok && !*abort_v; ++r) {
-                const int s = r % WS, hb = r & 1;
-                if (!mbar_wait(bar(B_WF + s), (r / WS) & 1, WAIT_NS)) { give_up(); ok = false; break; }
+                const int hb = r & 1;
                 if (r >= 2 && !mbar_wait(bar(B_HE + hb), ((r >> 1) - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
-                tc_fence_after();
-                const uint64_t wo = (uint64_t)(s * W_STAGE) >> 4;
                 const uint32_t th = tmem + COL_H13 + hb * 128;
+                for (int qd = 0; qd < NQ && ok; ++qd) {
+                    const int i = r * NQ + qd, s = i % CSLOTS;
+                    if (!mbar_wait(bar(B_CF + s), (i / CSLOTS) & 1, WAIT_NS)) { give_up(); ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t co = (uint64_t)(s * BOX) >> 4, qo = (uint64_t)(qd * BOX) >> 4;
 #pragma unroll
-                for (int j = 0; j < D / 16; ++j) {
-                    const uint64_t ko = (uint64_t)((j >> 2) * BOX + (j & 3) * 32) >> 4;
-                    mma_bf16(th, dQ + ko, dWc + wo + ko, i_h, j > 0 ? 1u : 0u);
+                    for (int j = 0; j < 4; ++j)
+                        mma_bf16(th, dQ + qo + j * 2, dC + co + j * 2, i_h, (qd > 0 || j > 0) ? 1u : 0u);
+                    mma_commit(bar(B_CE + s));
                 }
+                if (!ok) break;
                 mma_commit(bar(B_HF + hb));
-                // With one W stage the next block's weights load only after
-                // this block's output GEMM; with two, that GEMM trails by one.
-                const int ro = WS == 1 ? r : r - 1;
-                if (ro >= 0 && !out_mma(ro)) { give_up(); ok = false; break; }
+                if (r >= 1 && !out_mma(r - 1)) { give_up(); ok = false; break; }
             }
-            if (WS > 1 && ok && !*abort_v && R > 0 && !out_mma(R - 1)) give_up();
+            if (ok && !*abort_v && R > 0 && !out_mma(R - 1)) give_up();
             mma_commit(bar(B_O));
             mma_commit(bar(B_DRAIN));
             mbar_wait(bar(B_DRAIN), 0, WAIT_NS);
@@ -207,6 +235,7 @@ k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_HE + s));
+            // u = silu(h1) h3, with sigmoid(x) = 0.5 tanh(x / 2) + 0.5
             uint32_t pu[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
@@ -214,12 +243,13 @@ k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const float x1 = __uint_as_float(h1[j + t]);
-                    uu[t] = __fdividef(x1, 1.0f + __expf(-x1)) * __uint_as_float(h3[j + t]);
+                    const float sg = fmaf(0.5f, tanh_approx(0.5f * x1), 0.5f);
+                    uu[t] = x1 * sg * __uint_as_float(h3[j + t]);
                 }
                 pu[j / 2] = pack_bf16(uu[0], uu[1]);
             }
             if (r >= 2 && !mbar_wait_warp(bar(B_UE + s), ((r >> 1) - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
-            unsigned char* ub = sm + OFF_U + s * BOX;
+            unsigned char* ub = sm + Lo::OFF_U + s * BOX;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<uint4*>(ub + sw128_offset(row, hf * 32 + c * 8)) =
@@ -268,7 +298,7 @@ bool apply_tc_supported(const lact_state* st) {
            tmap_available();
 }
 
-template <int D, int WS>
+template <int D>
 static cudaError_t launch_apply_d(const lact_state* st, TokView q, void* o, cudaStream_t s) {
     const int dh = st->cfg.dh, BH = st->BH;
     CUtensorMap mq, m1, m3, m2;
@@ -294,19 +324,19 @@ static cudaError_t launch_apply_d(const lact_state* st, TokView q, void* o, cuda
     aa.BH = BH;
     aa.dh = dh;
     aa.status = st->status;
-    constexpr uint32_t smem = ApplyLayout<D, WS>::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(k_apply_tc<D, WS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    constexpr uint32_t smem = ApplyLayout<D>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(k_apply_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((q.n + TT - 1) / TT), BH);
-    k_apply_tc<D, WS><<<grid, NTHREADS, smem, s>>>(mq, m1, m3, m2, aa);
+    k_apply_tc<D><<<grid, NTHREADS, smem, s>>>(mq, m1, m3, m2, aa);
     g_launches++;
     g_tc_launches++;
     return cudaGetLastError();
 }
 
 cudaError_t launch_apply_tc(const lact_state* st, TokView q, void* o, cudaStream_t s) {
-    if (st->cfg.d == 128) return launch_apply_d<128, 2>(st, q, o, s);
-    return launch_apply_d<256, 1>(st, q, o, s);
+    if (st->cfg.d == 128) return launch_apply_d<128>(st, q, o, s);
+    return launch_apply_d<256>(st, q, o, s);
 }
 
 }  // namespace lact
