@@ -131,7 +131,7 @@ class Workload:
     dh: int
     dtype: str          # "f32" or "bf16": dtype of q, k, v and o
     order: str          # "causal" (apply-then-update per chunk) or "set" (update-then-apply)
-    opt: str            # "gd" or "muon"
+    opt: str            # "gd", "muon" or "momentum"
     n_kv: int           # update tokens per (b, h)
     n_q: int            # query tokens per (b, h)
     chunk: int          # tokens per update chunk
@@ -141,6 +141,7 @@ class Workload:
     ns_b: float = -4.7750
     ns_c: float = 2.0315
     muon_lr: float = 0.02
+    momentum: float = 0.9
 
     @property
     def bf16(self) -> bool:
@@ -159,7 +160,8 @@ class Workload:
 
 # The five workloads: two tiny fp32 causal layers (GD, Muon), a language-model
 # shaped causal layer (32K tokens in 2,048-token chunks), the 48-view image-set
-# layer (196,608 update tokens, 4,096 queries) and the million-token set layer.
+# layer (196,608 update tokens, 4,096 queries) and the million-token set layer;
+# then the momentum update rule on the tiny fp32 and the language-model shapes.
 WORKLOADS = {
     1: Workload(1, "tiny-causal-f32-gd", 1, 2, 64, 128, "f32", "causal", "gd",
                 2048, 2048, 512, BASE_SEED + 1),
@@ -171,6 +173,10 @@ WORKLOADS = {
                 196608, 4096, 196608, BASE_SEED + 4),
     5: Workload(5, "million-token-set-bf16-muon", 1, 8, 128, 512, "bf16", "set", "muon",
                 1048576, 65536, 1048576, BASE_SEED + 5),
+    6: Workload(6, "tiny-causal-f32-momentum", 1, 2, 64, 128, "f32", "causal", "momentum",
+                2048, 2048, 512, BASE_SEED + 6),
+    7: Workload(7, "lm-causal-bf16-momentum", 2, 4, 256, 512, "bf16", "causal", "momentum",
+                32768, 32768, 2048, BASE_SEED + 7),
 }
 
 

@@ -28,6 +28,8 @@ that prose (each choice is listed in the design notes):
   f_W(x) = W2 (silu(W1 x) * (W3 x)),   W1, W3: [dh, d],  W2: [d, dh]
   L      = - sum_i eta_i <f_W(k_i), v_i>            (one chunk)
   GD:    W <- W - dL/dW                              (step size lives in eta)
+  momentum: M <- beta M + dL/dW (M starts at 0 and carries across chunks),
+         W <- W - M, per matrix (beta = 0.9)
   Muon:  W <- W - lr * NS5(dL/dW)   per matrix,  NS5 = five quintic
          Newton-Schulz steps with (a, b, c) = (3.4445, -4.7750, 2.0315) on
          the Frobenius-normalised gradient (eps 1e-7), on the orientation
@@ -46,6 +48,7 @@ import numpy as np
 NS_A, NS_B, NS_C = 3.4445, -4.7750, 2.0315
 NS_EPS = 1e-7
 MUON_LR = 0.02
+MOMENTUM_BETA = 0.9
 
 
 # --------------------------------------------------------------------------
@@ -162,12 +165,22 @@ def renorm_update(W, delta):
     return Wt * scale[:, None]
 
 
+def momentum_velocity(M, g, beta: float = MOMENTUM_BETA):
+    """Heavy-ball momentum (review page, "Local attention and nonlinear memory
+    work together": gradient descent, momentum and Muon are the update rules
+    compared): the velocity after this chunk, beta M + g."""
+    return beta * M + g
+
+
 def chunk_update(W, K, V, eta, opt: str, lr: float = MUON_LR, ns_steps: int = 5,
-                 a: float = NS_A, b: float = NS_B, c: float = NS_C, token_slice: int | None = None):
+                 a: float = NS_A, b: float = NS_B, c: float = NS_C, token_slice: int | None = None,
+                 mom=None, beta: float = MOMENTUM_BETA):
     """One update of the fast weights W = (W1, W2, W3) on one chunk.
 
     token_slice only bounds memory: the chunk gradient is the sum over tokens,
     so it is taken slice by slice and added up before the single optimiser step.
+    For opt == "momentum", `mom` is the list of the three velocities; it is
+    replaced in place by the new ones and the step is -velocity.
     """
     W1, W2, W3 = W
     n = K.shape[0]
@@ -179,8 +192,16 @@ def chunk_update(W, K, V, eta, opt: str, lr: float = MUON_LR, ns_steps: int = 5,
         e = min(n, s + step)
         d1, d2, d3 = chunk_gradient(W1, W2, W3, K[s:e], V[s:e], eta[s:e])
         g1 += d1; g2 += d2; g3 += d3
+    if opt == "momentum":
+        for m, g in enumerate((g1, g2, g3)):
+            mom[m] = momentum_velocity(mom[m], g, beta)
+        return tuple(renorm_update(Wm, -Mm) for Wm, Mm in zip(W, mom))
     return tuple(renorm_update(Wm, optimizer_delta(g, opt, lr, ns_steps, a, b, c))
                  for Wm, g in ((W1, g1), (W2, g2), (W3, g3)))
+
+
+def zero_velocity(W):
+    return [np.zeros_like(Wm) for Wm in W]
 
 
 # --------------------------------------------------------------------------
@@ -191,6 +212,8 @@ def sequence_causal(W, Q, K, V, eta, chunk: int, opt: str, **kw):
     Returns (O [n, d], final W)."""
     n = Q.shape[0]
     O = np.zeros_like(Q)
+    if opt == "momentum":
+        kw = dict(kw, mom=zero_velocity(W))
     for s in range(0, n, chunk):
         e = min(n, s + chunk)
         O[s:e] = fast_weight_apply(W[0], W[1], W[2], Q[s:e])
@@ -200,6 +223,8 @@ def sequence_causal(W, Q, K, V, eta, chunk: int, opt: str, **kw):
 
 def sequence_set(W, Q, K, V, eta, opt: str, **kw):
     """Update-then-apply: one update on all input tokens, then read the queries."""
+    if opt == "momentum":
+        kw = dict(kw, mom=zero_velocity(W))
     W = chunk_update(W, K, V, eta, opt, **kw)
     return fast_weight_apply(W[0], W[1], W[2], Q), W
 
@@ -214,7 +239,7 @@ def run_workload(w, inp, heads=None, token_slice: int | None = None):
     heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     O = np.zeros((B, H, w.n_q, w.d))
     W1 = np.zeros((B, H, w.dh, w.d)); W2 = np.zeros((B, H, w.d, w.dh)); W3 = np.zeros((B, H, w.dh, w.d))
-    kw = dict(lr=w.muon_lr, ns_steps=w.ns_steps, a=w.ns_a, b=w.ns_b, c=w.ns_c)
+    kw = dict(lr=w.muon_lr, ns_steps=w.ns_steps, a=w.ns_a, b=w.ns_b, c=w.ns_c, beta=w.momentum)
     for (b, h) in heads:
         W0 = (inp.W1[h].astype(np.float64), inp.W2[h].astype(np.float64), inp.W3[h].astype(np.float64))
         Q, K, V = as_f64(inp.q[b, h]), as_f64(inp.k[b, h]), as_f64(inp.v[b, h])

@@ -266,3 +266,48 @@ def test_set_mode_is_update_then_apply_and_slices_sum():
     np.testing.assert_allclose(o, O.fast_weight_apply(*Wu, Q), rtol=0, atol=0)
     o2, W2f = O.sequence_set((W1, W2, W3), Q, K, V, eta, opt="muon", token_slice=7)
     np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------------------- momentum
+def _chunks(seed, n_chunks=3, chunk=5, d=4, dh=8):
+    W1, W2, W3, _, _, _ = _tiny(d=d, dh=dh, n=1, seed=seed)
+    g = np.random.default_rng(seed + 100)
+    K = g.normal(size=(n_chunks * chunk, d))
+    V = g.normal(size=(n_chunks * chunk, d))
+    eta = 0.02 + 0.01 * g.random(n_chunks * chunk)
+    return (W1, W2, W3), K, V, eta
+
+
+def test_momentum_with_zero_beta_is_gradient_descent():
+    W, K, V, eta = _chunks(7)
+    o_m, W_m = O.sequence_causal(W, K, K, V, eta, 5, "momentum", beta=0.0)
+    o_g, W_g = O.sequence_causal(W, K, K, V, eta, 5, "gd")
+    np.testing.assert_array_equal(o_m, o_g)
+    for a, b in zip(W_m, W_g):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_momentum_step_is_geometric_sum_of_past_chunk_gradients():
+    # Unrolled: the step after chunk c is -sum_{j <= c} beta^(c-j) g_j, with
+    # g_j the chunk gradient at the weights chunk j read. Rebuild the
+    # trajectory from that closed sum and compare with the oracle's run.
+    beta, chunk = 0.9, 5
+    W, K, V, eta = _chunks(8, n_chunks=4, chunk=chunk)
+    _, W_final = O.sequence_causal(W, K, K, V, eta, chunk, "momentum", beta=beta)
+    Wc, grads = W, []
+    for c in range(4):
+        sl = slice(c * chunk, (c + 1) * chunk)
+        grads.append(O.chunk_gradient(*Wc, K[sl], V[sl], eta[sl]))
+        step = [-sum(beta ** (c - j) * grads[j][m] for j in range(c + 1)) for m in range(3)]
+        Wc = tuple(O.renorm_update(Wc[m], step[m]) for m in range(3))
+    for a, b in zip(W_final, Wc):
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def test_momentum_first_chunk_equals_gradient_descent():
+    # the velocity starts at zero: after one chunk momentum and GD agree for any beta
+    W, K, V, eta = _chunks(9, n_chunks=1)
+    _, W_m = O.sequence_causal(W, K, K, V, eta, 5, "momentum", beta=0.9)
+    _, W_g = O.sequence_causal(W, K, K, V, eta, 5, "gd")
+    for a, b in zip(W_m, W_g):
+        np.testing.assert_array_equal(a, b)
