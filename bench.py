@@ -301,7 +301,7 @@ def main():
     q, k, v, e = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, he))
     W1, W2, W3 = (torch.from_numpy(x).to(dev) for x in (inp.W1, inp.W2, inp.W3))
     cfg = L.make_config(w.B, w.H, w.d, w.dh, w.dtype, w.opt, max_chunk=w.chunk, ns_steps=w.ns_steps,
-                        ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr)
+                        ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr, momentum=w.momentum)
     layer = L.LactLayer(cfg, W1, W2, W3, device=dev)
     order = L.LACT_CAUSAL_APPLY_THEN_UPDATE if w.order == "causal" else L.LACT_SET_UPDATE_THEN_APPLY
     o = torch.empty_like(q)

@@ -1,7 +1,9 @@
 // Update + row renormalisation of the fast weights, and their bf16 shadow.
 //
 //   W~_j = W_j + scale * D_j            (GD: D = dL/dW, scale = -1;
-//                                        Muon: D = NS5(dL/dW), scale = -lr)
+//                                        Muon: D = NS5(dL/dW), scale = -lr;
+//                                        momentum: M = beta M + dL/dW kept,
+//                                        D = M, scale = -1)
 //   W'_j = W~_j * ||W_j|| / ||W~_j||     for every row j of W1, W2, W3
 //
 // (LaCT review page, "Local attention and nonlinear memory work together":
@@ -22,6 +24,8 @@ struct UpdArgs {
     R* W[3];
     const R* D[3];
     bf16* S[3];        // bf16 shadows (nullptr: none)
+    R* Mo[3];          // momentum velocities (nullptr: none), updated in place
+    R beta;
     int rows[3];       // rows per head of each matrix
     int len[3];        // row length of each matrix
     int BH;
@@ -69,6 +73,7 @@ __global__ void __launch_bounds__(256) k_update_renorm(UpdArgs<R> a) {
     const int len = a.len[m];
     R* w = a.W[m] + row * len;
     const R* dv = a.D[m] + row * len;
+    R* mo = a.Mo[m] ? a.Mo[m] + row * len : nullptr;
     // Pass 1: both norms. Rows are at most 1024 long: keep them in registers.
     constexpr int MAXV = 1024 / (32 * VEC);
     R wt[MAXV][VEC];
@@ -80,6 +85,13 @@ __global__ void __launch_bounds__(256) k_update_renorm(UpdArgs<R> a) {
             R wv[VEC], gv[VEC];
             load_vec(w + c, wv, VEC);
             load_vec(dv + c, gv, VEC);
+            if (mo) {
+                R mv[VEC];
+                load_vec(mo + c, mv, VEC);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) gv[k] = fma_r(a.beta, mv[k], gv[k]);
+                store_vec(mo + c, gv, VEC);
+            }
 #pragma unroll
             for (int k = 0; k < VEC; ++k) {
                 const R t = fma_r(a.scale, gv[k], wv[k]);
@@ -133,18 +145,21 @@ __global__ void k_convert(const A* __restrict__ src, B* __restrict__ dst, size_t
 }
 
 template <typename R>
-cudaError_t update_t(const lact_state* st, const void* const g[3], double scale, cudaStream_t s) {
+cudaError_t update_t(const lact_state* st, const void* const g[3], double scale, void* const mom[3], double beta,
+                     cudaStream_t s) {
     UpdArgs<R> a;
     const int d = st->cfg.d, dh = st->cfg.dh;
     for (int m = 0; m < 3; ++m) {
         a.W[m] = static_cast<R*>(st->W[m]);
         a.D[m] = static_cast<const R*>(g[m]);
         a.S[m] = st->cfg.io_dtype == LACT_BF16 ? st->Wsh[m] : nullptr;
+        a.Mo[m] = mom ? static_cast<R*>(mom[m]) : nullptr;
         a.rows[m] = m == 1 ? d : dh;
         a.len[m] = m == 1 ? dh : d;
     }
     a.BH = st->BH;
     a.scale = (R)scale;
+    a.beta = (R)beta;
     a.status = st->status;
     const int64_t rows = (int64_t)st->BH * (2 * dh + d);
     const int blocks = (int)((rows * 32 + 255) / 256);
@@ -157,8 +172,9 @@ cudaError_t update_t(const lact_state* st, const void* const g[3], double scale,
 
 }  // namespace
 
-cudaError_t launch_update(const lact_state* st, const void* const g[3], double scale, cudaStream_t s) {
-    return st->f64 ? update_t<double>(st, g, scale, s) : update_t<float>(st, g, scale, s);
+cudaError_t launch_update(const lact_state* st, const void* const g[3], double scale, void* const mom[3],
+                          double beta, cudaStream_t s) {
+    return st->f64 ? update_t<double>(st, g, scale, mom, beta, s) : update_t<float>(st, g, scale, mom, beta, s);
 }
 
 cudaError_t launch_shadow(const lact_state* st, cudaStream_t s) {

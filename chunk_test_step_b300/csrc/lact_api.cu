@@ -24,7 +24,8 @@ static bool config_ok(const lact_config* c) {
     if (!(c->d == 32 || c->d == 64 || c->d == 128 || c->d == 256)) return false;
     if (c->dh < 64 || c->dh > 1024 || c->dh % 64 != 0) return false;
     if (c->io_dtype != LACT_F32 && c->io_dtype != LACT_BF16) return false;
-    if (c->opt != LACT_OPT_GD && c->opt != LACT_OPT_MUON) return false;
+    if (c->opt != LACT_OPT_GD && c->opt != LACT_OPT_MUON && c->opt != LACT_OPT_MOMENTUM) return false;
+    if (c->opt == LACT_OPT_MOMENTUM && !(c->momentum >= 0.0 && c->momentum < 1.0)) return false;
     if (c->opt == LACT_OPT_MUON && (c->ns_steps < 1 || c->ns_steps > 16)) return false;
     if (c->max_chunk < 1 || c->max_chunk > (1LL << 40)) return false;
     return true;
@@ -56,6 +57,7 @@ WsLayout ws_layout(const lact_config& c) {
     L.ns[2] = take(3 * BH * mm * mm * rs);
     L.ns[3] = take(3 * BH * mm * mm * rs);
     L.inter = take((size_t)3 * BH * slice_cap(c) * c.dh * 2);
+    for (int m = 0; m < 3; ++m) L.mom[m] = take(c.opt == LACT_OPT_MOMENTUM ? mat * rs : 0);
     L.status = take(64 * 4);
     L.total = off;
     return L;
@@ -174,7 +176,8 @@ static lact_status do_step(lact_state* st, void* const g[3], cudaStream_t s) {
     }
     PhaseTimer t(st, LACT_PHASE_UPDATE, s);
     const void* gc[3] = {g[0], g[1], g[2]};
-    cudaError_t e = launch_update(st, gc, scale, s);
+    const bool mom = st->cfg.opt == LACT_OPT_MOMENTUM;
+    cudaError_t e = launch_update(st, gc, scale, mom ? st->mom : nullptr, st->cfg.momentum, s);
     t.done();
     return cuda_status(e);
 }
@@ -216,6 +219,7 @@ lact_status lact_init_state(lact_state** out, const lact_config* cfg, void* d_ws
     st->partial = st->ws + L.partial;
     for (int i = 0; i < 4; ++i) st->ns[i] = st->ws + L.ns[i];
     st->inter = reinterpret_cast<bf16*>(st->ws + L.inter);
+    for (int m = 0; m < 3; ++m) st->mom[m] = cfg->opt == LACT_OPT_MOMENTUM ? st->ws + L.mom[m] : nullptr;
     st->slice_cap = slice_cap(*cfg);
     st->status = reinterpret_cast<int*>(st->ws + L.status);
     st->last_stream = s;
@@ -231,6 +235,8 @@ lact_status lact_init_state(lact_state** out, const lact_config* cfg, void* d_ws
     const size_t per_head = (size_t)cfg->d * cfg->dh;
     const float* src[3] = {d_W1, d_W2, d_W3};
     cudaError_t e = cudaMemsetAsync(st->status, 0, 64 * 4, s);
+    for (int m = 0; m < 3 && e == cudaSuccess; ++m)
+        if (st->mom[m]) e = cudaMemsetAsync(st->mom[m], 0, per_head * cfg->B * cfg->H * st->rsize, s);
     for (int m = 0; m < 3 && e == cudaSuccess; ++m)
         for (int b = 0; b < cfg->B && e == cudaSuccess; ++b)
             e = launch_convert(src[m], false, static_cast<char*>(st->W[m]) + (size_t)b * cfg->H * per_head * st->rsize,
@@ -368,17 +374,21 @@ lact_status lact_set_weights(lact_state* st, const float* d_W1, const float* d_W
     return cuda_status(launch_shadow(st, s));
 }
 
+// The master weights, then (momentum) their velocities.
+static void* state_part(const lact_state* st, int i) { return i < 3 ? st->W[i] : st->mom[i - 3]; }
+static int state_parts(const lact_state* st) { return st->cfg.opt == LACT_OPT_MOMENTUM ? 6 : 3; }
+
 size_t lact_state_bytes(const lact_state* st) {
     if (!st) return 0;
-    return 3 * (size_t)st->BH * st->cfg.d * st->cfg.dh * st->rsize;
+    return (size_t)state_parts(st) * st->BH * st->cfg.d * st->cfg.dh * st->rsize;
 }
 
 lact_status lact_export_state(const lact_state* st, void* d_dst, size_t bytes, cudaStream_t s) {
     if (!st || !d_dst || bytes < lact_state_bytes(st)) return LACT_ERR_INVALID_ARG;
-    const size_t one = lact_state_bytes(st) / 3;
-    for (int m = 0; m < 3; ++m)
-        if (cudaMemcpyAsync(static_cast<char*>(d_dst) + m * one, st->W[m], one, cudaMemcpyDeviceToDevice, s) !=
-            cudaSuccess)
+    const size_t one = lact_state_bytes(st) / state_parts(st);
+    for (int m = 0; m < state_parts(st); ++m)
+        if (cudaMemcpyAsync(static_cast<char*>(d_dst) + m * one, state_part(st, m), one, cudaMemcpyDeviceToDevice,
+                            s) != cudaSuccess)
             return LACT_ERR_CUDA;
     return LACT_OK;
 }
@@ -386,10 +396,10 @@ lact_status lact_export_state(const lact_state* st, void* d_dst, size_t bytes, c
 lact_status lact_import_state(lact_state* st, const void* d_src, size_t bytes, cudaStream_t s) {
     if (!st || !d_src || bytes != lact_state_bytes(st)) return LACT_ERR_INVALID_ARG;
     st->last_stream = s;
-    const size_t one = bytes / 3;
-    for (int m = 0; m < 3; ++m)
-        if (cudaMemcpyAsync(st->W[m], static_cast<const char*>(d_src) + m * one, one, cudaMemcpyDeviceToDevice, s) !=
-            cudaSuccess)
+    const size_t one = bytes / state_parts(st);
+    for (int m = 0; m < state_parts(st); ++m)
+        if (cudaMemcpyAsync(state_part(st, m), static_cast<const char*>(d_src) + m * one, one,
+                            cudaMemcpyDeviceToDevice, s) != cudaSuccess)
             return LACT_ERR_CUDA;
     return cuda_status(launch_shadow(st, s));
 }

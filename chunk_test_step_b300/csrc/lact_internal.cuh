@@ -27,6 +27,7 @@ struct WsLayout {
     size_t partial;    // real split-K partials [kMaxSlots][3][BH][dh*d]
     size_t ns[4];      // real Newton-Schulz scratch: X, X', A, B over 3*BH matrices
     size_t inter;      // bf16 per-token dh1, dh3, u' of one token slice [3][BH][slice_cap][dh] (two-kernel gradient)
+    size_t mom[3];     // real momentum velocities, same layouts as W (momentum only)
     size_t status;     // int32[64]: [0] sticky status bits, [1..] diagnostics
     size_t total;
 };
@@ -57,6 +58,7 @@ struct lact_state {
     void* partial;
     void* ns[4];
     lact::bf16* inter;
+    void* mom[3];             // momentum velocities (nullptr unless the rule is momentum)
     int64_t slice_cap;
     int* status;
     cudaStream_t last_stream;
@@ -143,7 +145,10 @@ cudaError_t launch_wgrad_tc(const lact_state* st, TokView k, TokView v, const bf
 cudaError_t launch_reduce(const lact_state* st, int slots, bool accumulate, void* const out[3],
                           cudaStream_t s);
 cudaError_t launch_newton_schulz(const lact_state* st, void* const g[3], cudaStream_t s);
-cudaError_t launch_update(const lact_state* st, const void* const g[3], double scale, cudaStream_t s);
+// W <- renorm(W + scale D) per row, D = g, or with velocities (mom != nullptr)
+// M <- beta M + g and D = M.
+cudaError_t launch_update(const lact_state* st, const void* const g[3], double scale, void* const mom[3],
+                          double beta, cudaStream_t s);
 cudaError_t launch_shadow(const lact_state* st, cudaStream_t s);
 // Raw-pointer forms of the bf16-io SIMT gradient and its reduction (no state).
 cudaError_t launch_grad_simt_bf16_raw(int d, int dh, int BH, const float* W1, const float* W2, const float* W3,

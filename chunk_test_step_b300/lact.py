@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "liblact.so")
 
 LACT_OK, LACT_ERR_INVALID_ARG, LACT_ERR_UNSUPPORTED, LACT_ERR_CUDA, LACT_ERR_TIMEOUT, LACT_ERR_NONFINITE = range(6)
 LACT_F32, LACT_BF16 = 0, 1
-LACT_OPT_GD, LACT_OPT_MUON = 0, 1
+LACT_OPT_GD, LACT_OPT_MUON, LACT_OPT_MOMENTUM = 0, 1, 2
 LACT_CAUSAL_APPLY_THEN_UPDATE, LACT_SET_UPDATE_THEN_APPLY = 0, 1
 PHASES = ("apply", "grad", "reduce", "ns", "update")
 
@@ -34,7 +34,7 @@ class lact_config(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("d", ctypes.c_int), ("dh", ctypes.c_int),
                 ("io_dtype", ctypes.c_int), ("opt", ctypes.c_int), ("ns_steps", ctypes.c_int),
                 ("ns_a", ctypes.c_double), ("ns_b", ctypes.c_double), ("ns_c", ctypes.c_double),
-                ("muon_lr", ctypes.c_double), ("max_chunk", ctypes.c_int64)]
+                ("muon_lr", ctypes.c_double), ("max_chunk", ctypes.c_int64), ("momentum", ctypes.c_double)]
 
 
 class lact_profile(ctypes.Structure):
@@ -121,11 +121,13 @@ def lact_status_str(status: int) -> str:
     return load().lact_status_str(status).decode()
 
 
+_OPTS = {"gd": LACT_OPT_GD, "muon": LACT_OPT_MUON, "momentum": LACT_OPT_MOMENTUM}
+
+
 def make_config(B, H, d, dh, io_dtype="bf16", opt="gd", max_chunk=1 << 20, ns_steps=5,
-                ns_a=3.4445, ns_b=-4.7750, ns_c=2.0315, muon_lr=0.02) -> lact_config:
-    return lact_config(B, H, d, dh, LACT_BF16 if io_dtype == "bf16" else LACT_F32,
-                       LACT_OPT_MUON if opt == "muon" else LACT_OPT_GD, ns_steps,
-                       ns_a, ns_b, ns_c, muon_lr, max_chunk)
+                ns_a=3.4445, ns_b=-4.7750, ns_c=2.0315, muon_lr=0.02, momentum=0.9) -> lact_config:
+    return lact_config(B, H, d, dh, LACT_BF16 if io_dtype == "bf16" else LACT_F32, _OPTS[opt], ns_steps,
+                       ns_a, ns_b, ns_c, muon_lr, max_chunk, momentum)
 
 
 def lact_workspace_bytes(cfg: lact_config) -> int:

@@ -53,7 +53,9 @@ typedef enum {
 } lact_status;
 
 typedef enum { LACT_F32 = 0, LACT_BF16 = 1 } lact_dtype;
-typedef enum { LACT_OPT_GD = 0, LACT_OPT_MUON = 1 } lact_opt;
+/* Update rules (review page, "Local attention and nonlinear memory work
+ * together": gradient descent, momentum and Muon are the rules compared). */
+typedef enum { LACT_OPT_GD = 0, LACT_OPT_MUON = 1, LACT_OPT_MOMENTUM = 2 } lact_opt;
 typedef enum { LACT_CAUSAL_APPLY_THEN_UPDATE = 0, LACT_SET_UPDATE_THEN_APPLY = 1 } lact_order;
 
 typedef struct {
@@ -68,6 +70,9 @@ typedef struct {
     double ns_a, ns_b, ns_c; /* quintic coefficients, (3.4445, -4.7750, 2.0315) */
     double muon_lr;     /* Muon step size, 0.02 */
     int64_t max_chunk;  /* most tokens one lact_chunk_update / chunk of lact_sequence may hold */
+    double momentum;    /* LACT_OPT_MOMENTUM: heavy-ball coefficient beta in [0, 1), 0.9. Per
+                           matrix a velocity M (zero at lact_init_state) carries across updates:
+                           M <- beta M + dL/dW, then W <- renorm(W - M) */
 } lact_config;
 
 typedef struct lact_state lact_state;   /* opaque host-side handle */
@@ -75,7 +80,8 @@ typedef struct lact_state lact_state;   /* opaque host-side handle */
 /* Per-phase device time, filled by lact_get_profile() when profiling is on. */
 typedef enum {
     LACT_PHASE_APPLY = 0,    /* readout kernel(s) */
-    LACT_PHASE_GRAD = 1,     /* fused forward-on-keys + backward + weight-gradient kernel */
+    LACT_PHASE_GRAD = 1,     /* chunk gradient: the fused kernel (head dim 128), or per token
+                                slice the per-token kernel + weight-gradient GEMMs (256) */
     LACT_PHASE_REDUCE = 2,   /* split-K partial-sum reduction */
     LACT_PHASE_NS = 3,       /* Newton-Schulz (Muon) */
     LACT_PHASE_UPDATE = 4,   /* update + row renorm + bf16 shadow */
@@ -132,20 +138,22 @@ lact_status lact_chunk_gradient(lact_state* st, const void* d_k, const void* d_v
                                 float* d_dW2, float* d_dW3, cudaStream_t stream);
 
 /* Optimiser step + row renorm from a given gradient (same layouts as above):
- * W <- renorm(W - dW) for GD, renorm(W - lr NS5(dW)) for Muon. */
+ * W <- renorm(W - dW) for GD, renorm(W - lr NS5(dW)) for Muon, and for
+ * momentum M <- beta M + dW, W <- renorm(W - M). */
 lact_status lact_apply_gradient(lact_state* st, const float* d_dW1, const float* d_dW2,
                                 const float* d_dW3, cudaStream_t stream);
 
 /* Copy the fp32 fast weights out / in: d_W1 [B,H,dh,d], d_W2 [B,H,d,dh],
- * d_W3 [B,H,dh,d]. lact_set_weights also refreshes the bf16 shadow. This is
- * the state a caller checkpoints to resume a sequence. */
+ * d_W3 [B,H,dh,d]. lact_set_weights also refreshes the bf16 shadow and
+ * leaves the momentum velocities as they are. */
 lact_status lact_get_weights(const lact_state* st, float* d_W1, float* d_W2, float* d_W3,
                              cudaStream_t stream);
 lact_status lact_set_weights(lact_state* st, const float* d_W1, const float* d_W2,
                              const float* d_W3, cudaStream_t stream);
 
-/* The resumable state in its own precision (the master fast weights: fp32
- * for bf16 io, fp64 for fp32 io), for exact checkpoint / resume.
+/* The resumable state in its own precision (the master fast weights, then
+ * for momentum their velocities: fp32 for bf16 io, fp64 for fp32 io), for
+ * exact checkpoint / resume.
  * lact_state_bytes gives the size; export copies it to d_dst, import copies
  * it back from d_src (a buffer written by lact_export_state of a state with
  * the same configuration) and refreshes the bf16 shadow. */

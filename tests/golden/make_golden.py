@@ -1,12 +1,13 @@
 """Write the sampled full-size expected values of tests/test_gpu_fullsize.py.
 
 Runs the fp64 oracle (oracle/) on the full-size bf16 workloads (the
-language-model causal layer, the 48-view image-set layer and the
-million-token set layer) with the seeded inputs of lact_inputs, and stores,
+language-model causal layers with GD and with momentum, the 48-view
+image-set layer and the million-token set layer) with the seeded inputs of
+lact_inputs, and stores,
 per (b, h), a fixed random sample of rows of the output o and of the final
 fast weights W1, W2, W3. Nothing here comes from the CUDA path.
 
-    python tests/golden/make_golden.py [workload numbers, default 2 4 5]
+    python tests/golden/make_golden.py [workload numbers, default 2 4 5 7]
 
 Takes minutes (the million-token layer is ~6.6e12 fp64 FLOP).
 """
@@ -67,4 +68,4 @@ def main(nums):
 
 
 if __name__ == "__main__":
-    main([int(x) for x in sys.argv[1:]] or [2, 4, 5])
+    main([int(x) for x in sys.argv[1:]] or [2, 4, 5, 7])

@@ -41,7 +41,7 @@ def config_for(w: li.Workload, max_chunk: int | None = None):
     from chunk_test_step_b300 import lact as L
     return L.make_config(w.B, w.H, w.d, w.dh, w.dtype, w.opt,
                          max_chunk=max_chunk or max(w.chunk, 1), ns_steps=w.ns_steps,
-                         ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr)
+                         ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr, momentum=w.momentum)
 
 
 def run_gpu(w: li.Workload, inp: li.Inputs):

@@ -39,6 +39,15 @@ def test_workspace_bytes():
         assert L.lact_workspace_bytes(bad) == 0
 
 
+def test_momentum_rule_holds_its_velocities_in_the_workspace():
+    gd = L.make_config(1, 8, 128, 512, "bf16", "gd", max_chunk=4096)
+    mo = L.make_config(1, 8, 128, 512, "bf16", "momentum", max_chunk=4096, momentum=0.9)
+    mat = 8 * 128 * 512
+    assert L.lact_workspace_bytes(mo) >= L.lact_workspace_bytes(gd) + 3 * mat * 4
+    for beta in (-0.1, 1.0, float("nan")):
+        assert L.lact_workspace_bytes(L.make_config(1, 8, 128, 512, "bf16", "momentum", momentum=beta)) == 0
+
+
 def test_bad_arguments_are_rejected_on_the_host():
     lib = L.load()
     c = L.make_config(1, 2, 64, 128, "f32", "gd", max_chunk=512)

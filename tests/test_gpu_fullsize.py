@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
-@pytest.mark.parametrize("num", [1, 3])
+@pytest.mark.parametrize("num", [1, 3, 6])
 def test_tiny_workloads_full_size(num):
     w = li.WORKLOADS[num]
     inp = li.make_inputs(w)
@@ -33,7 +33,7 @@ def test_tiny_workloads_full_size(num):
     assert max(errs.values()) < TOL[w.dtype], errs
 
 
-@pytest.mark.parametrize("num", [2, 4, 5])
+@pytest.mark.parametrize("num", [2, 4, 5, 7])
 def test_bf16_workloads_full_size_sampled(num):
     import torch
     from chunk_test_step_b300 import lact as L

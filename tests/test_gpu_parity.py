@@ -35,6 +35,8 @@ SMALL = {
     3: dict(n_kv=2048),
     4: dict(n_kv=5000 + 13, n_q=333),
     5: dict(n_kv=8192 + 77, n_q=500),
+    6: dict(n_kv=2048),                       # the whole tiny momentum workload
+    7: dict(n_kv=2 * 2048 + 301),
 }
 
 
@@ -129,8 +131,36 @@ def test_apply_gradient_matches_oracle(num, opt):
                                            np.linalg.norm(W0[m][h].astype(np.float64), axis=1), rtol=2e-6)
 
 
+@pytest.mark.parametrize("num", [6, 7])
+def test_momentum_velocity_carries_across_two_steps(num):
+    # two optimiser steps from given gradients: the second moves by
+    # beta * (first gradient) + (second gradient), then renorm
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[num].with_tokens(128, seed=li.WORKLOADS[num].seed + 3100)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    shapes = ((w.dh, w.d), (w.d, w.dh), (w.dh, w.d))
+    s = w.seed + 3100
+    G = [[li.normal(s, 30 + 3 * k + m, (w.B, w.H) + sh, scale=0.05) for m, sh in enumerate(shapes)] for k in range(2)]
+    for k in range(2):
+        L.lact_apply_gradient(layer.handle, *(to_device(x) for x in G[k]))
+    got = [to_host_f64(x) for x in layer.weights()]
+    torch.cuda.synchronize()
+    W0 = (inp.W1, inp.W2, inp.W3)
+    for b in range(w.B):
+        for h in range(w.H):
+            for m in range(3):
+                M = O.momentum_velocity(np.zeros(shapes[m]), G[0][m][b, h].astype(np.float64), w.momentum)
+                Wm = O.renorm_update(W0[m][h].astype(np.float64), -M)
+                M = O.momentum_velocity(M, G[1][m][b, h].astype(np.float64), w.momentum)
+                Wm = O.renorm_update(Wm, -M)
+                err = rel_l2(got[m][b, h], Wm)
+                assert err < TOL[w.dtype], (m, b, h, err)
+
+
 # ------------------------------------------------- whole layer calls (a8)
-@pytest.mark.parametrize("num", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("num", [1, 2, 3, 4, 5, 6, 7])
 def test_sequence_matches_oracle(num):
     w = _small(num)
     inp = li.make_inputs(w)
@@ -181,7 +211,7 @@ def test_update_beyond_max_chunk_is_rejected():
     assert ex.value.status == L.LACT_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("num", [3, 2])
+@pytest.mark.parametrize("num", [3, 2, 6, 7])
 def test_checkpoint_resume_equals_one_run(num):
     torch = _torch()
     from chunk_test_step_b300 import lact as L
@@ -239,7 +269,7 @@ def test_profiling_counts_phases():
     assert all(prof[p]["ms"] > 0 for p in prof)
 
 
-@pytest.mark.parametrize("num", [2, 4, 5])
+@pytest.mark.parametrize("num", [2, 4, 5, 7])
 def test_bf16_workloads_run_on_tensor_core_kernels(num):
     # every launch of the readout and gradient phases of the bf16 layers is a
     # tcgen05 kernel (no CUDA-core stand-in)
