@@ -78,12 +78,14 @@ def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
 def flops(w: li.Workload) -> dict:
     """Algorithmic FLOP of one layer call (per the method, no recompute)."""
     BH, d, dh = w.B * w.H, w.d, w.dh
-    if w.order == "causal":
-        upd, app, chunks = 12 * d * dh * w.n_kv * BH, 6 * d * dh * w.n_q * BH, -(-w.n_kv // w.chunk)
+    chunks = -(-w.n_kv // w.chunk) if w.order == "causal" else 1
+    if w.memory == "linear":
+        # o = W q: 2 d^2 per query; dW = -(eta V)^T K: 2 d^2 per update token
+        upd, app, nmat = 2 * d * d * w.n_kv * BH, 2 * d * d * w.n_q * BH, 1
     else:
-        upd, app, chunks = 12 * d * dh * w.n_kv * BH, 6 * d * dh * w.n_q * BH, 1
+        upd, app, nmat = 12 * d * dh * w.n_kv * BH, 6 * d * dh * w.n_q * BH, 3
     m, n = min(d, dh), max(d, dh)
-    ns = (5 * (4 * m * m * n + 2 * m ** 3) * 3 * BH * chunks) if w.opt == "muon" else 0
+    ns = (5 * (4 * m * m * n + 2 * m ** 3) * nmat * BH * chunks) if w.opt == "muon" else 0
     return {"update": upd, "apply": app, "ns": ns, "total": upd + app + ns}
 
 
@@ -299,9 +301,10 @@ def main():
     inp = li.make_inputs(w)
     hq, hk, hv, he = pinned_inputs(w, inp)
     q, k, v, e = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, he))
-    W1, W2, W3 = (torch.from_numpy(x).to(dev) for x in (inp.W1, inp.W2, inp.W3))
+    W1, W2, W3 = (None if x is None else torch.from_numpy(x).to(dev) for x in (inp.W1, inp.W2, inp.W3))
     cfg = L.make_config(w.B, w.H, w.d, w.dh, w.dtype, w.opt, max_chunk=w.chunk, ns_steps=w.ns_steps,
-                        ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr, momentum=w.momentum)
+                        ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr, momentum=w.momentum,
+                        memory=w.memory)
     layer = L.LactLayer(cfg, W1, W2, W3, device=dev)
     order = L.LACT_CAUSAL_APPLY_THEN_UPDATE if w.order == "causal" else L.LACT_SET_UPDATE_THEN_APPLY
     o = torch.empty_like(q)
@@ -399,7 +402,14 @@ def main():
     grad_flop = fl["update"] / chunks
     achieved = grad_flop / (grad_ms / 1e3) / 1e12
     tensor = grad["tensor_launches"] > 0
-    if tensor:
+    if w.memory == "linear":
+        # the linear memory's gradient reads k, v (and eta) once for 2 d^2 FLOP a token: HBM-bound
+        esz = 2 if w.dtype == "bf16" else 4
+        grad_bytes = w.B * w.H * (w.n_kv / chunks) * (2 * w.d * esz + 4)
+        achieved = grad_bytes / (grad_ms / 1e3) / 1e9
+        peak, bound, note = pk["hbm_gbs"], "hbm", f"HBM copy bandwidth, {pk_src}"
+        kernel = "k_wgrad_tc (linear, -eta V scaled in shared memory)" if tensor else "k_lin_grad_simt"
+    elif tensor:
         peak, bound, note = pk["bf16_tflops"], "tensor", f"dense bf16 burst, {pk_src}"
         kernel = "k_grad_tc" if w.d == 128 else "k_fwdbwd_tc + k_wgrad_tc"
     else:
@@ -407,7 +417,8 @@ def main():
         peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
         bound, note = "alu", "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"
         kernel = "k_grad_simt"
-    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": achieved / peak,
             "traffic": measured_traffic(w, reduced), "traffic_unit": "bytes per launch", "kernel": kernel,
             "peak_source": note, "ms_per_launch": grad_ms, "flop_per_launch": grad_flop,
             "launches_per_call": grad["launches"] / max(1, grad["calls"])}

@@ -76,14 +76,18 @@ __global__ void k_ns_unpack(const R* __restrict__ X, R* __restrict__ g0, R* __re
 
 // Batched C = alpha * rnd(A) rnd(op(B)) + beta * Cin, all row-major fp32.
 // A: [M, K]; B: [K, N] (transB = 0) or [N, K] (transB = 1); rnd = bf16 rounding.
-// 64 x 64 output tile per CTA, 256 threads, 4 x 4 outputs per thread.
-constexpr int BM = 64, BN = 64, BK = 16;
+// (16 TPT) x (16 TPT) output tile per CTA, 256 threads, TPT x TPT outputs per
+// thread; every output sums over k in order, so the tile size does not change
+// the result. TPT = 1 gives small matrices (the fp32-io layers' 64 x 64
+// products) enough CTAs to spread over the GPU.
+constexpr int BK = 16;
 
-template <typename R>
+template <typename R, int TPT>
 __global__ void __launch_bounds__(256) k_bgemm(const R* __restrict__ A, const R* __restrict__ B,
                                                const R* __restrict__ Cin, R* __restrict__ C,
                                                int M, int N, int K, size_t sA, size_t sB, size_t sC,
                                                int transB, R alpha, R beta) {
+    constexpr int BM = 16 * TPT, BN = 16 * TPT;
     __shared__ R As[BK][BM + 4];
     __shared__ R Bs[BK][BN + 4];
     const int bz = blockIdx.z;
@@ -91,11 +95,11 @@ __global__ void __launch_bounds__(256) k_bgemm(const R* __restrict__ A, const R*
     if (Cin) Cin += bz * sC;
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
-    R acc[4][4];
+    R acc[TPT][TPT];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < TPT; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = R(0);
+        for (int j = 0; j < TPT; ++j) acc[i][j] = R(0);
     for (int k0 = 0; k0 < K; k0 += BK) {
         for (int i = tid; i < BM * BK; i += 256) {
             const int r = i / BK, kk = i % BK;
@@ -113,20 +117,20 @@ __global__ void __launch_bounds__(256) k_bgemm(const R* __restrict__ A, const R*
         __syncthreads();
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
-            R a[4], b[4];
+            R a[TPT], b[TPT];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty + 16 * i]; b[i] = Bs[kk][tx + 16 * i]; }
+            for (int i = 0; i < TPT; ++i) { a[i] = As[kk][ty + 16 * i]; b[i] = Bs[kk][tx + 16 * i]; }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < TPT; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fma_r(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < TPT; ++j) acc[i][j] = fma_r(a[i], b[j], acc[i][j]);
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < TPT; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < TPT; ++j) {
             const int gm = m0 + ty + 16 * i, gn = n0 + tx + 16 * j;
             if (gm < M && gn < N) {
                 const size_t o = (size_t)gm * N + gn;
@@ -141,8 +145,15 @@ template <typename R>
 cudaError_t bgemm(const R* A, const R* B, const R* Cin, R* C, int M, int N, int K,
                   size_t sA, size_t sB, size_t sC, int transB, R alpha, R beta, int batch,
                   cudaStream_t s) {
-    dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM, batch);
-    k_bgemm<R><<<grid, 256, 0, s>>>(A, B, Cin, C, M, N, K, sA, sB, sC, transB, alpha, beta);
+    // 64 x 64 tiles when they alone give a few waves of CTAs, else 16 x 16
+    const int64_t big = (int64_t)((N + 63) / 64) * ((M + 63) / 64) * batch;
+    if (big >= 4 * 148) {
+        dim3 grid((N + 63) / 64, (M + 63) / 64, batch);
+        k_bgemm<R, 4><<<grid, 256, 0, s>>>(A, B, Cin, C, M, N, K, sA, sB, sC, transB, alpha, beta);
+    } else {
+        dim3 grid((N + 15) / 16, (M + 15) / 16, batch);
+        k_bgemm<R, 1><<<grid, 256, 0, s>>>(A, B, Cin, C, M, N, K, sA, sB, sC, transB, alpha, beta);
+    }
     g_launches++;
     return cudaGetLastError();
 }
@@ -154,7 +165,7 @@ cudaError_t ns_t(const lact_state* st, void* const gv[3], cudaStream_t s) {
     sh.d = c.d; sh.dh = c.dh; sh.BH = st->BH;
     sh.m = c.d < c.dh ? c.d : c.dh;
     sh.n = c.d < c.dh ? c.dh : c.d;
-    const int batch = 3 * st->BH;
+    const int batch = st->nmat * st->BH;
     R* g[3] = {static_cast<R*>(gv[0]), static_cast<R*>(gv[1]), static_cast<R*>(gv[2])};
     R* X = static_cast<R*>(st->ns[0]);
     R* X2 = static_cast<R*>(st->ns[1]);

@@ -208,9 +208,9 @@ __global__ void __launch_bounds__(NT) k_grad_simt(TokView k, TokView v, const fl
 
 // out[m] (+)= sum over slots s = 0, 1, ... of partial[s][m], in that order.
 template <typename R>
-__global__ void k_reduce(const R* __restrict__ partial, int slots, size_t mat, bool accumulate,
+__global__ void k_reduce(const R* __restrict__ partial, int slots, size_t mat, int nmat, bool accumulate,
                          R* __restrict__ o0, R* __restrict__ o1, R* __restrict__ o2) {
-    const size_t n = 3 * mat;
+    const size_t n = (size_t)nmat * mat;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const int m = (int)(i / mat);
         const size_t j = i - (size_t)m * mat;
@@ -307,14 +307,15 @@ cudaError_t launch_grad_simt(const lact_state* st, TokView k, TokView v, const f
 
 cudaError_t launch_reduce(const lact_state* st, int slots, bool accumulate, void* const out[3], cudaStream_t s) {
     const size_t mat = (size_t)st->BH * st->cfg.dh * st->cfg.d;
-    const size_t want = (3 * mat + 255) / 256, cap = (size_t)st->num_sms * 8;
+    const size_t want = (st->nmat * mat + 255) / 256, cap = (size_t)st->num_sms * 8;
     const int blocks = (int)(want < cap ? want : cap);
     if (st->f64)
-        k_reduce<double><<<blocks, 256, 0, s>>>(static_cast<const double*>(st->partial), slots, mat, accumulate,
+        k_reduce<double><<<blocks, 256, 0, s>>>(static_cast<const double*>(st->partial), slots, mat, st->nmat,
+                                                accumulate,
                                                 static_cast<double*>(out[0]), static_cast<double*>(out[1]),
                                                 static_cast<double*>(out[2]));
     else
-        k_reduce<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(st->partial), slots, mat, accumulate,
+        k_reduce<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(st->partial), slots, mat, st->nmat, accumulate,
                                                static_cast<float*>(out[0]), static_cast<float*>(out[1]),
                                                static_cast<float*>(out[2]));
     g_launches++;
@@ -371,7 +372,7 @@ cudaError_t launch_reduce_f32_raw(const float* partial, int slots, size_t mat, f
                                   int num_sms, cudaStream_t s) {
     const size_t want = (3 * mat + 255) / 256, cap = (size_t)num_sms * 8;
     const int blocks = (int)(want < cap ? want : cap);
-    k_reduce<float><<<blocks, 256, 0, s>>>(partial, slots, mat, false, o0, o1, o2);
+    k_reduce<float><<<blocks, 256, 0, s>>>(partial, slots, mat, 3, false, o0, o1, o2);
     g_launches++;
     return cudaGetLastError();
 }

@@ -394,7 +394,7 @@ cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s)
     if (e != cudaSuccess) return e;
     const int cs = a.n / CB;
     cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3((unsigned)(cs * 3 * st->BH));
+    lc.gridDim = dim3((unsigned)(cs * st->nmat * st->BH));
     lc.blockDim = dim3(NTHREADS);
     lc.dynamicSmemBytes = SMEM_BYTES;
     lc.stream = s;

@@ -10,9 +10,15 @@
 //   dW2 = V^T u'       [d x dh]
 // Each is C (+)= A^T B summed over the tokens, with A and B stored
 // token-major (row = token), so both are MN-major operands. One CTA computes
-// a 128 x NB tile of one product for one head over all tokens of the slice
-// (no split over tokens, so no partial sums), with a 4-deep TMA pipeline of
-// 64-token stages and the fp32 accumulator in TMEM.
+// a 128 x NB tile of one product for one head over the tokens of its split
+// (one split here: no partial sums), with a 4-deep TMA pipeline of 64-token
+// stages and the fp32 accumulator in TMEM.
+//
+// The same kernel forms the chunk gradient of the linear fast-weight memory,
+// dW = -(eta V)^T K (LaCT review page, Fig. 8: the linear state): there the
+// epilogue warps scale every token row of the A tile (V) by -eta in shared
+// memory before the MMAs read it, and the tokens are split over CTAs whose
+// partial sums a fixed-order reduction adds.
 //
 // Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
 // issues the MMAs (one thread), warps 2..5 write the tile out (thread = row
@@ -38,7 +44,7 @@ constexpr uint32_t STAGE_BYTES = A_BYTES + (NBMAX / 64) * BOXB;   // 48 KB
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-enum { B_F = 0, B_E = STAGES, B_ACC = 2 * STAGES, B_DRAIN, NBARS };
+enum { B_F = 0, B_E = STAGES, B_S = 2 * STAGES, B_ACC = 3 * STAGES, B_DRAIN, NBARS };
 
 // One product C (+)= A^T B of one head. The tensor maps cover all heads:
 // A: (ma inner, tokens, heads), B: (nb inner, tokens, heads).
@@ -56,6 +62,10 @@ struct WArgs {
     int ntok;            // tokens in the slice
     int accumulate;      // add to C instead of overwriting it
     int* status;
+    const float* eta;    // nullptr, or: scale A's token rows by -eta (head h at eta + h * eta_n_total + eta_t0)
+    int64_t eta_n_total, eta_t0;
+    int toks_per_split;  // tokens per split (grid z); a multiple of 64
+    size_t split_stride; // elements between the C of consecutive splits
 };
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -79,7 +89,11 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
     const int mb = t / n_blocks, nbk = t % n_blocks;
     const CUtensorMap* tma = which == 0 ? &ta0 : which == 1 ? &ta1 : &ta2;
     const CUtensorMap* tmb = which == 0 ? &tb0 : which == 1 ? &tb1 : &tb2;
-    const int nsteps = (a.ntok + TK - 1) / TK;
+    const int split = blockIdx.z;
+    const int tok0 = split * a.toks_per_split;                       // first token of this split
+    const int tok1 = min(a.ntok, tok0 + a.toks_per_split);
+    const int nsteps = tok1 > tok0 ? (tok1 - tok0 + TK - 1) / TK : 0;
+    const bool scale = a.eta != nullptr;
     const uint32_t base = smem_u32(sm);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -89,6 +103,7 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(B_F + s), 1);
             mbar_init(bar(B_E + s), 1);
+            mbar_init(bar(B_S + s), 4);
         }
         mbar_init(bar(B_ACC), 1);
         mbar_init(bar(B_DRAIN), 1);
@@ -123,9 +138,9 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
                 const uint32_t st = base + s * STAGE_BYTES;
                 mbar_expect_tx(bar(B_F + s), bytes);
                 for (int c = 0; c < TM / 64; ++c)
-                    tma_load_3d(st + c * BOXB, tma, bar(B_F + s), mb * TM + c * 64, P.a_t0 + i * TK, h);
+                    tma_load_3d(st + c * BOXB, tma, bar(B_F + s), mb * TM + c * 64, P.a_t0 + tok0 + i * TK, h);
                 for (int c = 0; c < NB / 64; ++c)
-                    tma_load_3d(st + A_BYTES + c * BOXB, tmb, bar(B_F + s), nbk * NB + c * 64, P.b_t0 + i * TK, h);
+                    tma_load_3d(st + A_BYTES + c * BOXB, tmb, bar(B_F + s), nbk * NB + c * 64, P.b_t0 + tok0 + i * TK, h);
                 issued = i + 1;
             }
             for (int i = max(0, issued - STAGES); i < issued; ++i)
@@ -139,7 +154,7 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
             bool ok = true;
             for (int i = 0; i < nsteps && ok && !*abort_v; ++i) {
                 const int s = i % STAGES;
-                if (!mbar_wait(bar(B_F + s), (i / STAGES) & 1, WAIT_NS)) { give_up(); ok = false; break; }
+                if (!mbar_wait(bar((scale ? B_S : B_F) + s), (i / STAGES) & 1, WAIT_NS)) { give_up(); ok = false; break; }
                 tc_fence_after();
                 const uint64_t so = (uint64_t)(s * STAGE_BYTES) >> 4;
 #pragma unroll
@@ -156,9 +171,40 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
         const int q = warp & 3;
         const int row = 32 * q + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        if (scale) {
+            // every token row of the A tile times -eta of its token (a swizzled
+            // row keeps its 128 bytes in place, so a whole row scales as one)
+            const int et = tid - 64;                    // 0..127: (64-element block, token row)
+            const int blk = et >> 6, trow = et & 63;
+            const float* eh = a.eta + (int64_t)h * a.eta_n_total + a.eta_t0;
+            for (int i = 0; i < nsteps; ++i) {
+                const int s = i % STAGES;
+                if (*abort_v || !mbar_wait_warp(bar(B_F + s), (i / STAGES) & 1, WAIT_NS)) { give_up(); break; }
+                const int tok = tok0 + i * TK + trow;
+                const float ne = tok < tok1 ? -eh[tok] : 0.0f;
+                uint4* rp = reinterpret_cast<uint4*>(sm + s * STAGE_BYTES + blk * BOXB + trow * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 x = rp[c];
+                    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&w[u]);
+                        float2 f = __bfloat1622float2(pr);
+                        pr = __floats2bfloat162_rn(f.x * ne, f.y * ne);
+                        w[u] = *reinterpret_cast<uint32_t*>(&pr);
+                    }
+                    rp[c] = x;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_S + s));
+            }
+        }
         if (!*abort_v && mbar_wait_warp(bar(B_ACC), 0, WAIT_NS)) {
             tc_fence_after();
-            float* crow = P.c + (size_t)h * P.ma * P.nb + (size_t)(mb * TM + row) * P.nb + nbk * NB;
+            float* crow = P.c + (size_t)split * a.split_stride + (size_t)h * P.ma * P.nb + (size_t)(mb * TM + row) * P.nb +
+                          nbk * NB;
             for (int c0 = 0; c0 < NB; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(lane_base + c0, v);
@@ -232,12 +278,71 @@ cudaError_t launch_wgrad_tc(const lact_state* st, TokView k, TokView v, const bf
     wa.ntok = ntok;
     wa.accumulate = accumulate ? 1 : 0;
     wa.status = st->status;
+    wa.eta = nullptr;
+    wa.eta_n_total = 0;
+    wa.eta_t0 = 0;
+    wa.toks_per_split = ntok > 0 ? (ntok + TK - 1) / TK * TK : TK;
+    wa.split_stride = 0;
     cudaError_t e = cudaFuncSetAttribute(k_wgrad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)total, (unsigned)BH);
+    dim3 grid((unsigned)total, (unsigned)BH, 1);
     k_wgrad_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(ma[0], mb[0], ma[1], mb[1], ma[2], mb[2], wa);
     g_launches++;
     g_tc_launches++;
+    return cudaGetLastError();
+}
+
+// Linear memory (bf16 io, d = 128): partial dW = -(eta V)^T K of tokens
+// [k.t0, k.t0 + k.n), one fp32 partial per token split into st->partial
+// ([split][BH][d][d]); *slots receives the number of splits.
+cudaError_t launch_lin_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots,
+                               cudaStream_t s) {
+    const int d = st->cfg.d, BH = st->BH;
+    CUtensorMap mv, mk;
+    const uint32_t box[3] = {64, TK, 1};
+    const uint64_t k_dims[3] = {(uint64_t)d, (uint64_t)k.n_total, (uint64_t)BH};
+    const uint64_t k_str[2] = {(uint64_t)d * 2, (uint64_t)k.n_total * d * 2};
+    const uint64_t v_dims[3] = {(uint64_t)d, (uint64_t)v.n_total, (uint64_t)BH};
+    const uint64_t v_str[2] = {(uint64_t)d * 2, (uint64_t)v.n_total * d * 2};
+    if (!make_tmap_bf16(&mv, v.p, 3, v_dims, v_str, box) || !make_tmap_bf16(&mk, k.p, 3, k_dims, k_str, box))
+        return cudaErrorInvalidValue;
+    WArgs wa;
+    wa.p[0].ma = d;
+    wa.p[0].nb = d;
+    wa.p[0].a_t0 = (int)v.t0;
+    wa.p[0].b_t0 = (int)k.t0;
+    wa.p[0].c = static_cast<float*>(st->partial);
+    wa.nb_tile[0] = d % 256 == 0 ? 256 : 128;
+    wa.tiles[0] = (d / TM) * (d / wa.nb_tile[0]);
+    for (int m = 1; m < 3; ++m) {
+        wa.p[m] = wa.p[0];
+        wa.nb_tile[m] = wa.nb_tile[0];
+        wa.tiles[m] = 0;
+    }
+    wa.ntok = (int)k.n;
+    wa.accumulate = 0;
+    wa.status = st->status;
+    wa.eta = eta;
+    wa.eta_n_total = k.n_total;
+    wa.eta_t0 = k.t0;
+    // token splits: about one wave of CTAs, whole 64-token stages, at most kMaxSlots
+    const int64_t steps = (k.n + TK - 1) / TK;
+    int64_t splits = st->num_sms / (BH * wa.tiles[0]);
+    if (splits > steps) splits = steps;
+    if (splits > kMaxSlots) splits = kMaxSlots;
+    if (splits < 1) splits = 1;
+    const int64_t sps = (steps + splits - 1) / splits;
+    splits = (steps + sps - 1) / sps;
+    if (splits < 1) splits = 1;
+    wa.toks_per_split = (int)(sps * TK);
+    wa.split_stride = (size_t)BH * d * d;
+    cudaError_t e = cudaFuncSetAttribute(k_wgrad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)wa.tiles[0], (unsigned)BH, (unsigned)splits);
+    k_wgrad_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(mv, mk, mv, mk, mv, mk, wa);
+    g_launches++;
+    g_tc_launches++;
+    *slots = (int)splits;
     return cudaGetLastError();
 }
 

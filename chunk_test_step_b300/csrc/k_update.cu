@@ -154,14 +154,14 @@ cudaError_t update_t(const lact_state* st, const void* const g[3], double scale,
         a.D[m] = static_cast<const R*>(g[m]);
         a.S[m] = st->cfg.io_dtype == LACT_BF16 ? st->Wsh[m] : nullptr;
         a.Mo[m] = mom ? static_cast<R*>(mom[m]) : nullptr;
-        a.rows[m] = m == 1 ? d : dh;
+        a.rows[m] = m >= st->nmat ? 0 : (m == 1 ? d : dh);   // the linear memory has W1 only
         a.len[m] = m == 1 ? dh : d;
     }
     a.BH = st->BH;
     a.scale = (R)scale;
     a.beta = (R)beta;
     a.status = st->status;
-    const int64_t rows = (int64_t)st->BH * (2 * dh + d);
+    const int64_t rows = (int64_t)st->BH * (a.rows[0] + a.rows[1] + a.rows[2]);
     const int blocks = (int)((rows * 32 + 255) / 256);
     // every row length here is a multiple of 32; float4 when a multiple of 128
     if (sizeof(R) == 4 && d % 128 == 0 && dh % 128 == 0) k_update_renorm<R, 4><<<blocks, 256, 0, s>>>(a);
@@ -180,7 +180,7 @@ cudaError_t launch_update(const lact_state* st, const void* const g[3], double s
 cudaError_t launch_shadow(const lact_state* st, cudaStream_t s) {
     if (st->cfg.io_dtype != LACT_BF16) return cudaSuccess;
     const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
-    for (int m = 0; m < 3; ++m) {
+    for (int m = 0; m < st->nmat; ++m) {
         k_shadow<<<st->num_sms * 4, 256, 0, s>>>(static_cast<const float*>(st->W[m]), st->Wsh[m], n);
         g_launches++;
     }

@@ -28,8 +28,17 @@ static bool config_ok(const lact_config* c) {
     if (c->opt == LACT_OPT_MOMENTUM && !(c->momentum >= 0.0 && c->momentum < 1.0)) return false;
     if (c->opt == LACT_OPT_MUON && (c->ns_steps < 1 || c->ns_steps > 16)) return false;
     if (c->max_chunk < 1 || c->max_chunk > (1LL << 40)) return false;
+    if (c->memory != LACT_MEM_SWIGLU && c->memory != LACT_MEM_LINEAR) return false;
+    if (c->memory == LACT_MEM_LINEAR) {
+        if (c->dh != c->d) return false;
+        const bool served = c->io_dtype == LACT_F32 ? c->d <= 128 : c->d == 128;
+        if (!served) return false;
+    }
     return true;
 }
+
+// Fast-weight matrices of the memory: W1, W2, W3 (SwiGLU) or W1 = W (linear).
+static int nmat_of(const lact_config& c) { return c.memory == LACT_MEM_LINEAR ? 1 : 3; }
 
 int64_t slice_cap(const lact_config& c) {
     if (c.io_dtype != LACT_BF16 || c.d != 256) return 0;
@@ -44,20 +53,21 @@ WsLayout ws_layout(const lact_config& c) {
     const size_t BH = (size_t)c.B * c.H;
     const size_t mat = BH * c.d * c.dh;
     const size_t rs = real_size(c);
+    const int nm = nmat_of(c);
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-    for (int m = 0; m < 3; ++m) L.W[m] = take(mat * rs);
-    for (int m = 0; m < 3; ++m) L.Wsh[m] = take(c.io_dtype == LACT_BF16 ? mat * 2 : 0);
-    for (int m = 0; m < 3; ++m) L.dW[m] = take(mat * rs);
-    L.partial = take((size_t)kMaxSlots * 3 * mat * rs);
+    for (int m = 0; m < 3; ++m) L.W[m] = take(m < nm ? mat * rs : 0);
+    for (int m = 0; m < 3; ++m) L.Wsh[m] = take(m < nm && c.io_dtype == LACT_BF16 ? mat * 2 : 0);
+    for (int m = 0; m < 3; ++m) L.dW[m] = take(m < nm ? mat * rs : 0);
+    L.partial = take((size_t)kMaxSlots * nm * mat * rs);
     const size_t mm = (size_t)(c.d < c.dh ? c.d : c.dh);
     const size_t nn = (size_t)(c.d < c.dh ? c.dh : c.d);
-    L.ns[0] = take(3 * BH * mm * nn * rs);
-    L.ns[1] = take(3 * BH * mm * nn * rs);
-    L.ns[2] = take(3 * BH * mm * mm * rs);
-    L.ns[3] = take(3 * BH * mm * mm * rs);
+    L.ns[0] = take(nm * BH * mm * nn * rs);
+    L.ns[1] = take(nm * BH * mm * nn * rs);
+    L.ns[2] = take(nm * BH * mm * mm * rs);
+    L.ns[3] = take(nm * BH * mm * mm * rs);
     L.inter = take((size_t)3 * BH * slice_cap(c) * c.dh * 2);
-    for (int m = 0; m < 3; ++m) L.mom[m] = take(c.opt == LACT_OPT_MOMENTUM ? mat * rs : 0);
+    for (int m = 0; m < 3; ++m) L.mom[m] = take(c.opt == LACT_OPT_MOMENTUM && m < nm ? mat * rs : 0);
     L.status = take(64 * 4);
     L.total = off;
     return L;
@@ -121,7 +131,9 @@ static lact_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LACT_O
 static lact_status do_apply(lact_state* st, TokView q, void* o, cudaStream_t s) {
     if (q.n == 0) return LACT_OK;
     PhaseTimer t(st, LACT_PHASE_APPLY, s);
-    cudaError_t e = apply_tc_supported(st) ? launch_apply_tc(st, q, o, s) : launch_apply_simt(st, q, o, s);
+    cudaError_t e = st->nmat == 1          ? launch_lin_apply(st, q, o, s)
+                    : apply_tc_supported(st) ? launch_apply_tc(st, q, o, s)
+                                             : launch_apply_simt(st, q, o, s);
     t.done();
     return cuda_status(e);
 }
@@ -132,12 +144,12 @@ static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* et
     if (k.n == 0) {
         if (!accumulate) {
             const size_t bytes = (size_t)st->BH * st->cfg.d * st->cfg.dh * st->rsize;
-            for (int m = 0; m < 3; ++m)
+            for (int m = 0; m < st->nmat; ++m)
                 if (cudaMemsetAsync(out[m], 0, bytes, s) != cudaSuccess) return LACT_ERR_CUDA;
         }
         return LACT_OK;
     }
-    if (fwdbwd_tc_supported(st) && st->slice_cap > 0) {
+    if (st->nmat == 3 && fwdbwd_tc_supported(st) && st->slice_cap > 0) {
         // two kernels per token slice; the GEMMs write (or add to) out[] directly
         PhaseTimer t(st, LACT_PHASE_GRAD, s);
         cudaError_t e = cudaSuccess;
@@ -153,8 +165,10 @@ static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* et
     int slots = 0;
     {
         PhaseTimer t(st, LACT_PHASE_GRAD, s);
-        cudaError_t e = grad_tc_supported(st) ? launch_grad_tc(st, k, v, eta, &slots, s)
-                                              : launch_grad_simt(st, k, v, eta, &slots, s);
+        cudaError_t e = st->nmat == 1        ? (lin_tc_supported(st) ? launch_lin_grad_tc(st, k, v, eta, &slots, s)
+                                                                     : launch_lin_grad_simt(st, k, v, eta, &slots, s))
+                        : grad_tc_supported(st) ? launch_grad_tc(st, k, v, eta, &slots, s)
+                                                : launch_grad_simt(st, k, v, eta, &slots, s);
         t.done();
         if (e != cudaSuccess) return LACT_ERR_CUDA;
     }
@@ -195,17 +209,26 @@ size_t lact_workspace_bytes(const lact_config* cfg) {
     return ws_layout(*cfg).total;
 }
 
+// The memory's weight (or gradient) pointers: 3 for SwiGLU, W1 alone for the
+// linear memory; non-null and 16-byte aligned.
+static bool mats_ok(int nm, const void* a, const void* b, const void* c) {
+    const void* p[3] = {a, b, c};
+    for (int m = 0; m < nm; ++m)
+        if (!p[m] || !aligned16(p[m])) return false;
+    return true;
+}
+
 lact_status lact_init_state(lact_state** out, const lact_config* cfg, void* d_ws, size_t ws_bytes,
                             const float* d_W1, const float* d_W2, const float* d_W3, cudaStream_t s) {
-    if (!out || !config_ok(cfg) || !d_ws || !d_W1 || !d_W2 || !d_W3) return LACT_ERR_INVALID_ARG;
-    if (((uintptr_t)d_ws & 255u) != 0 || !aligned16(d_W1) || !aligned16(d_W2) || !aligned16(d_W3))
-        return LACT_ERR_INVALID_ARG;
+    if (!out || !config_ok(cfg) || !d_ws) return LACT_ERR_INVALID_ARG;
+    if (((uintptr_t)d_ws & 255u) != 0 || !mats_ok(nmat_of(*cfg), d_W1, d_W2, d_W3)) return LACT_ERR_INVALID_ARG;
     WsLayout L = ws_layout(*cfg);
     if (ws_bytes < L.total) return LACT_ERR_INVALID_ARG;
     lact_state* st = new (std::nothrow) lact_state();
     if (!st) return LACT_ERR_CUDA;
     st->cfg = *cfg;
     st->BH = cfg->B * cfg->H;
+    st->nmat = nmat_of(*cfg);
     st->f64 = cfg->io_dtype == LACT_F32;
     st->rsize = real_size(*cfg);
     st->ws = static_cast<char*>(d_ws);
@@ -237,7 +260,7 @@ lact_status lact_init_state(lact_state** out, const lact_config* cfg, void* d_ws
     cudaError_t e = cudaMemsetAsync(st->status, 0, 64 * 4, s);
     for (int m = 0; m < 3 && e == cudaSuccess; ++m)
         if (st->mom[m]) e = cudaMemsetAsync(st->mom[m], 0, per_head * cfg->B * cfg->H * st->rsize, s);
-    for (int m = 0; m < 3 && e == cudaSuccess; ++m)
+    for (int m = 0; m < st->nmat && e == cudaSuccess; ++m)
         for (int b = 0; b < cfg->B && e == cudaSuccess; ++b)
             e = launch_convert(src[m], false, static_cast<char*>(st->W[m]) + (size_t)b * cfg->H * per_head * st->rsize,
                                st->f64, (size_t)cfg->H * per_head, st->num_sms, s);
@@ -288,27 +311,25 @@ lact_status lact_chunk_gradient(lact_state* st, const void* d_k, const void* d_v
                                 int64_t n_tok, float* d_dW1, float* d_dW2, float* d_dW3, cudaStream_t s) {
     lact_status r = check_update(st, d_k, d_v, d_eta, n_tok);
     if (r != LACT_OK) return r;
-    if (!d_dW1 || !d_dW2 || !d_dW3 || !aligned16(d_dW1) || !aligned16(d_dW2) || !aligned16(d_dW3))
-        return LACT_ERR_INVALID_ARG;
+    if (!mats_ok(st->nmat, d_dW1, d_dW2, d_dW3)) return LACT_ERR_INVALID_ARG;
     st->last_stream = s;
     r = do_grad(st, TokView{d_k, n_tok, 0, n_tok}, TokView{d_v, n_tok, 0, n_tok}, d_eta, false, st->dW, s);
     if (r != LACT_OK) return r;
     float* out[3] = {d_dW1, d_dW2, d_dW3};
     const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
-    for (int m = 0; m < 3; ++m)
+    for (int m = 0; m < st->nmat; ++m)
         if (launch_convert(st->dW[m], st->f64, out[m], false, n, st->num_sms, s) != cudaSuccess) return LACT_ERR_CUDA;
     return LACT_OK;
 }
 
 lact_status lact_apply_gradient(lact_state* st, const float* d_dW1, const float* d_dW2, const float* d_dW3,
                                 cudaStream_t s) {
-    if (!st || !d_dW1 || !d_dW2 || !d_dW3 || !aligned16(d_dW1) || !aligned16(d_dW2) || !aligned16(d_dW3))
-        return LACT_ERR_INVALID_ARG;
+    if (!st || !mats_ok(st->nmat, d_dW1, d_dW2, d_dW3)) return LACT_ERR_INVALID_ARG;
     st->last_stream = s;
     // The Muon step works in place, so take a copy into the state's own buffer.
     const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
     const float* src[3] = {d_dW1, d_dW2, d_dW3};
-    for (int m = 0; m < 3; ++m)
+    for (int m = 0; m < st->nmat; ++m)
         if (launch_convert(src[m], false, st->dW[m], st->f64, n, st->num_sms, s) != cudaSuccess) return LACT_ERR_CUDA;
     return do_step(st, st->dW, s);
 }
@@ -354,29 +375,28 @@ lact_status lact_sequence(lact_state* st, lact_order order, const void* d_q, int
 }
 
 lact_status lact_get_weights(const lact_state* st, float* d_W1, float* d_W2, float* d_W3, cudaStream_t s) {
-    if (!st || !d_W1 || !d_W2 || !d_W3) return LACT_ERR_INVALID_ARG;
+    if (!st || !mats_ok(st->nmat, d_W1, d_W2, d_W3)) return LACT_ERR_INVALID_ARG;
     const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
     float* dst[3] = {d_W1, d_W2, d_W3};
-    for (int m = 0; m < 3; ++m)
+    for (int m = 0; m < st->nmat; ++m)
         if (launch_convert(st->W[m], st->f64, dst[m], false, n, st->num_sms, s) != cudaSuccess) return LACT_ERR_CUDA;
     return LACT_OK;
 }
 
 lact_status lact_set_weights(lact_state* st, const float* d_W1, const float* d_W2, const float* d_W3,
                              cudaStream_t s) {
-    if (!st || !d_W1 || !d_W2 || !d_W3 || !aligned16(d_W1) || !aligned16(d_W2) || !aligned16(d_W3))
-        return LACT_ERR_INVALID_ARG;
+    if (!st || !mats_ok(st->nmat, d_W1, d_W2, d_W3)) return LACT_ERR_INVALID_ARG;
     st->last_stream = s;
     const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
     const float* src[3] = {d_W1, d_W2, d_W3};
-    for (int m = 0; m < 3; ++m)
+    for (int m = 0; m < st->nmat; ++m)
         if (launch_convert(src[m], false, st->W[m], st->f64, n, st->num_sms, s) != cudaSuccess) return LACT_ERR_CUDA;
     return cuda_status(launch_shadow(st, s));
 }
 
 // The master weights, then (momentum) their velocities.
-static void* state_part(const lact_state* st, int i) { return i < 3 ? st->W[i] : st->mom[i - 3]; }
-static int state_parts(const lact_state* st) { return st->cfg.opt == LACT_OPT_MOMENTUM ? 6 : 3; }
+static void* state_part(const lact_state* st, int i) { return i < st->nmat ? st->W[i] : st->mom[i - st->nmat]; }
+static int state_parts(const lact_state* st) { return st->cfg.opt == LACT_OPT_MOMENTUM ? 2 * st->nmat : st->nmat; }
 
 size_t lact_state_bytes(const lact_state* st) {
     if (!st) return 0;

@@ -47,6 +47,7 @@ struct PhaseEvents { cudaEvent_t a, b; int phase; int launches; int tensor_launc
 struct lact_state {
     lact_config cfg;
     int BH;
+    int nmat;                 // fast-weight matrices: 3 (SwiGLU: W1, W2, W3) or 1 (linear: W1 = W, d x d)
     bool f64;                 // internal arithmetic in fp64 (fp32 io) or fp32 (bf16 io)
     size_t rsize;             // bytes of one internal real
     char* ws;
@@ -138,6 +139,14 @@ cudaError_t launch_apply_tc(const lact_state* st, TokView q, void* o, cudaStream
 // Two-kernel chunk gradient (bf16 io, head dim 256): per-token dh1, dh3, u'
 // of a token slice, then the three weight-gradient GEMMs over the slice.
 bool fwdbwd_tc_supported(const lact_state* st);
+// Linear memory: readout (tensor cores at bf16 d = 128, else CUDA cores) and
+// the chunk gradient's partial sums into st->partial (one per token split).
+bool lin_tc_supported(const lact_state* st);
+cudaError_t launch_lin_apply(const lact_state* st, TokView q, void* o, cudaStream_t s);
+cudaError_t launch_lin_grad_simt(const lact_state* st, TokView k, TokView v, const float* eta, int* slots,
+                                 cudaStream_t s);
+cudaError_t launch_lin_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots,
+                               cudaStream_t s);
 cudaError_t launch_fwdbwd_tc(const lact_state* st, TokView k, TokView v, const float* eta, bf16* inter,
                              int64_t slice_cap, cudaStream_t s);
 cudaError_t launch_wgrad_tc(const lact_state* st, TokView k, TokView v, const bf16* inter, int64_t slice_cap,

@@ -19,6 +19,7 @@ LACT_OK, LACT_ERR_INVALID_ARG, LACT_ERR_UNSUPPORTED, LACT_ERR_CUDA, LACT_ERR_TIM
 LACT_F32, LACT_BF16 = 0, 1
 LACT_OPT_GD, LACT_OPT_MUON, LACT_OPT_MOMENTUM = 0, 1, 2
 LACT_CAUSAL_APPLY_THEN_UPDATE, LACT_SET_UPDATE_THEN_APPLY = 0, 1
+LACT_MEM_SWIGLU, LACT_MEM_LINEAR = 0, 1
 PHASES = ("apply", "grad", "reduce", "ns", "update")
 
 # Every symbol include/lact.h declares.
@@ -34,7 +35,8 @@ class lact_config(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("d", ctypes.c_int), ("dh", ctypes.c_int),
                 ("io_dtype", ctypes.c_int), ("opt", ctypes.c_int), ("ns_steps", ctypes.c_int),
                 ("ns_a", ctypes.c_double), ("ns_b", ctypes.c_double), ("ns_c", ctypes.c_double),
-                ("muon_lr", ctypes.c_double), ("max_chunk", ctypes.c_int64), ("momentum", ctypes.c_double)]
+                ("muon_lr", ctypes.c_double), ("max_chunk", ctypes.c_int64), ("momentum", ctypes.c_double),
+                ("memory", ctypes.c_int)]
 
 
 class lact_profile(ctypes.Structure):
@@ -125,9 +127,10 @@ _OPTS = {"gd": LACT_OPT_GD, "muon": LACT_OPT_MUON, "momentum": LACT_OPT_MOMENTUM
 
 
 def make_config(B, H, d, dh, io_dtype="bf16", opt="gd", max_chunk=1 << 20, ns_steps=5,
-                ns_a=3.4445, ns_b=-4.7750, ns_c=2.0315, muon_lr=0.02, momentum=0.9) -> lact_config:
+                ns_a=3.4445, ns_b=-4.7750, ns_c=2.0315, muon_lr=0.02, momentum=0.9, memory="swiglu") -> lact_config:
     return lact_config(B, H, d, dh, LACT_BF16 if io_dtype == "bf16" else LACT_F32, _OPTS[opt], ns_steps,
-                       ns_a, ns_b, ns_c, muon_lr, max_chunk, momentum)
+                       ns_a, ns_b, ns_c, muon_lr, max_chunk, momentum,
+                       LACT_MEM_LINEAR if memory == "linear" else LACT_MEM_SWIGLU)
 
 
 def lact_workspace_bytes(cfg: lact_config) -> int:
@@ -230,9 +233,13 @@ class LactLayer:
         self.io_dtype = torch.bfloat16 if cfg.io_dtype == LACT_BF16 else torch.float32
 
     def weights(self, stream=None):
+        """(W1, W2, W3) fp32 [B, H, ...]; for the linear memory (W, None, None)."""
         c = self.cfg
         dev = self.workspace.device
         W1 = torch.empty(c.B, c.H, c.dh, c.d, device=dev)
+        if c.memory == LACT_MEM_LINEAR:
+            lact_get_weights(self.handle, W1, None, None, stream)
+            return W1, None, None
         W2 = torch.empty(c.B, c.H, c.d, c.dh, device=dev)
         W3 = torch.empty(c.B, c.H, c.dh, c.d, device=dev)
         lact_get_weights(self.handle, W1, W2, W3, stream)

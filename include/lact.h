@@ -57,6 +57,13 @@ typedef enum { LACT_F32 = 0, LACT_BF16 = 1 } lact_dtype;
  * together": gradient descent, momentum and Muon are the rules compared). */
 typedef enum { LACT_OPT_GD = 0, LACT_OPT_MUON = 1, LACT_OPT_MOMENTUM = 2 } lact_opt;
 typedef enum { LACT_CAUSAL_APPLY_THEN_UPDATE = 0, LACT_SET_UPDATE_THEN_APPLY = 1 } lact_order;
+/* Fast-weight memory (review page, "Local attention and nonlinear memory work
+ * together" and Fig. 8): the three-matrix SwiGLU MLP, or one linear d x d
+ * matrix W read as o = W q, whose chunk gradient is -sum_i eta_i v_i k_i^T.
+ * The linear memory needs dh == d and lives in the W1 slot ([.., d, d]); every
+ * W2 / W3 / dW2 / dW3 argument is then unused and may be NULL. It is served
+ * for fp32 io at d = 32, 64, 128 and bf16 io at d = 128. */
+typedef enum { LACT_MEM_SWIGLU = 0, LACT_MEM_LINEAR = 1 } lact_memory;
 
 typedef struct {
     int B, H;           /* batch entries and heads; every (b, h) has its own W */
@@ -73,6 +80,7 @@ typedef struct {
     double momentum;    /* LACT_OPT_MOMENTUM: heavy-ball coefficient beta in [0, 1), 0.9. Per
                            matrix a velocity M (zero at lact_init_state) carries across updates:
                            M <- beta M + dL/dW, then W <- renorm(W - M) */
+    lact_memory memory; /* LACT_MEM_SWIGLU (W1, W2, W3) or LACT_MEM_LINEAR (W1 only) */
 } lact_config;
 
 typedef struct lact_state lact_state;   /* opaque host-side handle */

@@ -142,6 +142,7 @@ class Workload:
     ns_c: float = 2.0315
     muon_lr: float = 0.02
     momentum: float = 0.9
+    memory: str = "swiglu"   # "swiglu" (W1, W2, W3) or "linear" (one d x d matrix in W1)
 
     @property
     def bf16(self) -> bool:
@@ -161,7 +162,10 @@ class Workload:
 # The five workloads: two tiny fp32 causal layers (GD, Muon), a language-model
 # shaped causal layer (32K tokens in 2,048-token chunks), the 48-view image-set
 # layer (196,608 update tokens, 4,096 queries) and the million-token set layer;
-# then the momentum update rule on the tiny fp32 and the language-model shapes.
+# then the momentum update rule on the tiny fp32 and the language-model shapes,
+# a wider causal layer in the shape of a 3B language model (24 heads of 128,
+# 32,768 tokens in 4,096-token chunks, Muon); then the linear fast-weight
+# memory (one d x d matrix) on the tiny fp32 and the image-set shapes.
 WORKLOADS = {
     1: Workload(1, "tiny-causal-f32-gd", 1, 2, 64, 128, "f32", "causal", "gd",
                 2048, 2048, 512, BASE_SEED + 1),
@@ -177,6 +181,12 @@ WORKLOADS = {
                 2048, 2048, 512, BASE_SEED + 6),
     7: Workload(7, "lm-causal-bf16-momentum", 2, 4, 256, 512, "bf16", "causal", "momentum",
                 32768, 32768, 2048, BASE_SEED + 7),
+    8: Workload(8, "lm3b-causal-bf16-muon", 1, 24, 128, 512, "bf16", "causal", "muon",
+                32768, 32768, 4096, BASE_SEED + 8),
+    9: Workload(9, "tiny-causal-f32-linear-gd", 1, 2, 64, 64, "f32", "causal", "gd",
+                2048, 2048, 512, BASE_SEED + 9, memory="linear"),
+    10: Workload(10, "image-set-bf16-linear-muon", 1, 6, 128, 128, "bf16", "set", "muon",
+                 196608, 4096, 196608, BASE_SEED + 10, memory="linear"),
 }
 
 
@@ -186,9 +196,9 @@ class Inputs:
     k: np.ndarray      # [B,H,n_kv,d]
     v: np.ndarray      # [B,H,n_kv,d]
     eta: np.ndarray    # [B,H,n_kv]   float32
-    W1: np.ndarray     # [H,dh,d]     float32 (shared over the batch)
-    W2: np.ndarray     # [H,d,dh]
-    W3: np.ndarray     # [H,dh,d]
+    W1: np.ndarray     # [H,dh,d]     float32 (shared over the batch); linear memory: [H,d,d]
+    W2: np.ndarray     # [H,d,dh]     (None for the linear memory)
+    W3: np.ndarray     # [H,dh,d]     (None for the linear memory)
 
 
 def make_inputs(w: Workload) -> Inputs:
@@ -197,6 +207,8 @@ def make_inputs(w: Workload) -> Inputs:
     k = unit_rows(s, STREAM_K, (B, H, w.n_kv, d), bf16=w.bf16)
     v = normal(s, STREAM_V, (B, H, w.n_kv, d), bf16=w.bf16)
     et = eta(s, STREAM_ETA, (B, H, w.n_kv))
+    if w.memory == "linear":
+        return Inputs(q, k, v, et, normal(s, STREAM_W1, (H, d, d), scale=1.0 / np.sqrt(d)), None, None)
     W1 = normal(s, STREAM_W1, (H, dh, d), scale=1.0 / np.sqrt(d))
     W2 = normal(s, STREAM_W2, (H, d, dh), scale=1.0 / np.sqrt(dh))
     W3 = normal(s, STREAM_W3, (H, dh, d), scale=1.0 / np.sqrt(d))

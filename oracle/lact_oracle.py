@@ -107,6 +107,26 @@ def chunk_gradient(W1, W2, W3, K, V, eta):
 
 
 # --------------------------------------------------------------------------
+# Linear fast-weight memory: one d x d matrix W, o = W q (review page,
+# "Local attention and nonlinear memory work together" and Fig. 8: the
+# larger linear state that the smaller SwiGLU state is compared against).
+# --------------------------------------------------------------------------
+def linear_apply(W, X):
+    """o_i = W x_i for every row x_i of X [n, d]."""
+    return X @ W.T
+
+
+def linear_chunk_loss(W, K, V, eta):
+    """L = -sum_i eta_i <W k_i, v_i>."""
+    return -float(np.sum(eta * np.sum(linear_apply(W, K) * V, axis=1)))
+
+
+def linear_chunk_gradient(W, K, V, eta):
+    """dL/dW = -sum_i eta_i v_i k_i^T, as one GEMM over the chunk: [d, d]."""
+    return -(eta[:, None] * V).T @ K
+
+
+# --------------------------------------------------------------------------
 # Muon: Newton-Schulz orthogonalisation of a matrix gradient (review page,
 # "Local attention and nonlinear memory work together").
 # --------------------------------------------------------------------------
@@ -172,32 +192,43 @@ def momentum_velocity(M, g, beta: float = MOMENTUM_BETA):
     return beta * M + g
 
 
+def memory_gradient(W, K, V, eta):
+    """Chunk gradient of the memory W: (W1, W2, W3) SwiGLU or (W,) linear."""
+    if len(W) == 1:
+        return (linear_chunk_gradient(W[0], K, V, eta),)
+    return chunk_gradient(W[0], W[1], W[2], K, V, eta)
+
+
+def memory_apply(W, X):
+    """Readout of the memory W: (W1, W2, W3) SwiGLU or (W,) linear."""
+    return linear_apply(W[0], X) if len(W) == 1 else fast_weight_apply(W[0], W[1], W[2], X)
+
+
 def chunk_update(W, K, V, eta, opt: str, lr: float = MUON_LR, ns_steps: int = 5,
                  a: float = NS_A, b: float = NS_B, c: float = NS_C, token_slice: int | None = None,
                  mom=None, beta: float = MOMENTUM_BETA):
-    """One update of the fast weights W = (W1, W2, W3) on one chunk.
+    """One update of the fast weights W = (W1, W2, W3), or (W,) for the
+    linear memory, on one chunk.
 
     token_slice only bounds memory: the chunk gradient is the sum over tokens,
     so it is taken slice by slice and added up before the single optimiser step.
     For opt == "momentum", `mom` is the list of the three velocities; it is
     replaced in place by the new ones and the step is -velocity.
     """
-    W1, W2, W3 = W
     n = K.shape[0]
     step = n if not token_slice else token_slice
-    g1 = np.zeros_like(W1); g2 = np.zeros_like(W2); g3 = np.zeros_like(W3)
+    grads = [np.zeros_like(Wm) for Wm in W]
     for s in range(0, max(n, 1), max(step, 1)):
         if n == 0:
             break
         e = min(n, s + step)
-        d1, d2, d3 = chunk_gradient(W1, W2, W3, K[s:e], V[s:e], eta[s:e])
-        g1 += d1; g2 += d2; g3 += d3
+        for g, d in zip(grads, memory_gradient(W, K[s:e], V[s:e], eta[s:e])):
+            g += d
     if opt == "momentum":
-        for m, g in enumerate((g1, g2, g3)):
+        for m, g in enumerate(grads):
             mom[m] = momentum_velocity(mom[m], g, beta)
         return tuple(renorm_update(Wm, -Mm) for Wm, Mm in zip(W, mom))
-    return tuple(renorm_update(Wm, optimizer_delta(g, opt, lr, ns_steps, a, b, c))
-                 for Wm, g in ((W1, g1), (W2, g2), (W3, g3)))
+    return tuple(renorm_update(Wm, optimizer_delta(g, opt, lr, ns_steps, a, b, c)) for Wm, g in zip(W, grads))
 
 
 def zero_velocity(W):
@@ -216,7 +247,7 @@ def sequence_causal(W, Q, K, V, eta, chunk: int, opt: str, **kw):
         kw = dict(kw, mom=zero_velocity(W))
     for s in range(0, n, chunk):
         e = min(n, s + chunk)
-        O[s:e] = fast_weight_apply(W[0], W[1], W[2], Q[s:e])
+        O[s:e] = memory_apply(W, Q[s:e])
         W = chunk_update(W, K[s:e], V[s:e], eta[s:e], opt, **kw)
     return O, W
 
@@ -226,22 +257,29 @@ def sequence_set(W, Q, K, V, eta, opt: str, **kw):
     if opt == "momentum":
         kw = dict(kw, mom=zero_velocity(W))
     W = chunk_update(W, K, V, eta, opt, **kw)
-    return fast_weight_apply(W[0], W[1], W[2], Q), W
+    return memory_apply(W, Q), W
 
 
 def run_workload(w, inp, heads=None, token_slice: int | None = None):
     """Run a whole workload (lact_inputs.Workload + Inputs) head by head.
 
-    Returns O [B,H,n_q,d] and W1, W2, W3 [B,H,...] in fp64 (None for heads not
-    listed in `heads`, a list of (b, h))."""
+    Returns O [B,H,n_q,d] and W1, W2, W3 [B,H,...] in fp64 (heads not listed
+    in `heads`, a list of (b, h), stay zero). For the linear memory W1 is the
+    memory [B,H,d,d] and W2, W3 are None."""
     from lact_inputs import as_f64  # input widening only (bf16 bits -> fp64)
     B, H = w.B, w.H
     heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     O = np.zeros((B, H, w.n_q, w.d))
-    W1 = np.zeros((B, H, w.dh, w.d)); W2 = np.zeros((B, H, w.d, w.dh)); W3 = np.zeros((B, H, w.dh, w.d))
+    linear = w.memory == "linear"
+    W1 = np.zeros((B, H, w.d, w.d) if linear else (B, H, w.dh, w.d))
+    W2 = None if linear else np.zeros((B, H, w.d, w.dh))
+    W3 = None if linear else np.zeros((B, H, w.dh, w.d))
     kw = dict(lr=w.muon_lr, ns_steps=w.ns_steps, a=w.ns_a, b=w.ns_b, c=w.ns_c, beta=w.momentum)
     for (b, h) in heads:
-        W0 = (inp.W1[h].astype(np.float64), inp.W2[h].astype(np.float64), inp.W3[h].astype(np.float64))
+        if linear:
+            W0 = (inp.W1[h].astype(np.float64),)
+        else:
+            W0 = (inp.W1[h].astype(np.float64), inp.W2[h].astype(np.float64), inp.W3[h].astype(np.float64))
         Q, K, V = as_f64(inp.q[b, h]), as_f64(inp.k[b, h]), as_f64(inp.v[b, h])
         e = inp.eta[b, h].astype(np.float64)
         if w.order == "causal":
@@ -249,5 +287,7 @@ def run_workload(w, inp, heads=None, token_slice: int | None = None):
         else:
             o, Wf = sequence_set(W0, Q, K, V, e, w.opt, token_slice=token_slice, **kw)
         O[b, h] = o
-        W1[b, h], W2[b, h], W3[b, h] = Wf
+        W1[b, h] = Wf[0]
+        if not linear:
+            W2[b, h], W3[b, h] = Wf[1], Wf[2]
     return O, W1, W2, W3

@@ -1,13 +1,15 @@
 """Write the sampled full-size expected values of tests/test_gpu_fullsize.py.
 
 Runs the fp64 oracle (oracle/) on the full-size bf16 workloads (the
-language-model causal layers with GD and with momentum, the 48-view
-image-set layer and the million-token set layer) with the seeded inputs of
+language-model causal layers with GD and with momentum, the 3B-shaped
+causal layer, the 48-view image-set layer, the million-token set layer and
+the image-set layer with the linear memory)
+with the seeded inputs of
 lact_inputs, and stores,
 per (b, h), a fixed random sample of rows of the output o and of the final
 fast weights W1, W2, W3. Nothing here comes from the CUDA path.
 
-    python tests/golden/make_golden.py [workload numbers, default 2 4 5 7]
+    python tests/golden/make_golden.py [workload numbers, default 2 4 5 7 8 10]
 
 Takes minutes (the million-token layer is ~6.6e12 fp64 FLOP).
 """
@@ -38,6 +40,7 @@ def sample_indices(w: li.Workload):
             "W1": sorted(g.choice(w.dh, size=W_ROWS, replace=False).tolist()),
             "W2": sorted(g.choice(w.d, size=W_ROWS, replace=False).tolist()),
             "W3": sorted(g.choice(w.dh, size=W_ROWS, replace=False).tolist()),
+            # (the linear memory has W1 only, [d, d]: its rows come from the W1 draw)
         })
     return out
 
@@ -56,8 +59,8 @@ def main(nums):
                 "b": b, "h": h, "rows": sel,
                 "o": [[float(f"{x:.8e}") for x in Of[b, h, i]] for i in sel["o"]],
                 "W1": [[float(f"{x:.8e}") for x in W1[b, h, i]] for i in sel["W1"]],
-                "W2": [[float(f"{x:.8e}") for x in W2[b, h, i]] for i in sel["W2"]],
-                "W3": [[float(f"{x:.8e}") for x in W3[b, h, i]] for i in sel["W3"]],
+                "W2": [] if W2 is None else [[float(f"{x:.8e}") for x in W2[b, h, i]] for i in sel["W2"]],
+                "W3": [] if W3 is None else [[float(f"{x:.8e}") for x in W3[b, h, i]] for i in sel["W3"]],
             })
         doc = {"workload": w.name, "number": num, "seed": w.seed,
                "written_by": "tests/golden/make_golden.py (fp64 oracle)", "heads": heads}
@@ -68,4 +71,4 @@ def main(nums):
 
 
 if __name__ == "__main__":
-    main([int(x) for x in sys.argv[1:]] or [2, 4, 5, 7])
+    main([int(x) for x in sys.argv[1:]] or [2, 4, 5, 7, 8, 10])

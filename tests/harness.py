@@ -27,6 +27,8 @@ def max_rel_l2_per_head(got, want) -> float:
 
 def to_device(a: np.ndarray, device="cuda"):
     import torch
+    if a is None:
+        return None
     if a.dtype == np.uint16:
         return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
     return torch.from_numpy(np.ascontiguousarray(a)).to(device)
@@ -41,7 +43,8 @@ def config_for(w: li.Workload, max_chunk: int | None = None):
     from chunk_test_step_b300 import lact as L
     return L.make_config(w.B, w.H, w.d, w.dh, w.dtype, w.opt,
                          max_chunk=max_chunk or max(w.chunk, 1), ns_steps=w.ns_steps,
-                         ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr, momentum=w.momentum)
+                         ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr, momentum=w.momentum,
+                         memory=w.memory)
 
 
 def run_gpu(w: li.Workload, inp: li.Inputs):
@@ -56,11 +59,11 @@ def run_gpu(w: li.Workload, inp: li.Inputs):
     torch.cuda.synchronize()
     st = L.lact_sync_status(layer.handle)
     assert st == L.LACT_OK, L.lact_status_str(st)
-    out = tuple(to_host_f64(x) for x in (o, W1, W2, W3))
+    out = tuple(None if x is None else to_host_f64(x) for x in (o, W1, W2, W3))
     layer.close()
     return out
 
 
 def compare(w: li.Workload, got, want) -> dict:
     names = ("o", "W1", "W2", "W3")
-    return {n: max_rel_l2_per_head(g, r) for n, g, r in zip(names, got, want)}
+    return {n: max_rel_l2_per_head(g, r) for n, g, r in zip(names, got, want) if r is not None}

@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
-@pytest.mark.parametrize("num", [1, 3, 6])
+@pytest.mark.parametrize("num", [1, 3, 6, 9])
 def test_tiny_workloads_full_size(num):
     w = li.WORKLOADS[num]
     inp = li.make_inputs(w)
@@ -33,7 +33,7 @@ def test_tiny_workloads_full_size(num):
     assert max(errs.values()) < TOL[w.dtype], errs
 
 
-@pytest.mark.parametrize("num", [2, 4, 5, 7])
+@pytest.mark.parametrize("num", [2, 4, 5, 7, 8, 10])
 def test_bf16_workloads_full_size_sampled(num):
     import torch
     from chunk_test_step_b300 import lact as L
@@ -55,11 +55,15 @@ def test_bf16_workloads_full_size_sampled(num):
         err = rel_l2(got_o, np.array(head["o"]))
         assert err < TOL["bf16"], ("o", b, h, err)
         for m, name in enumerate(("W1", "W2", "W3")):
+            if W[m] is None:
+                continue
             got = W[m][b, h, rows[name]].double().cpu().numpy()
             err = rel_l2(got, np.array(head[name]))
             assert err < TOL["bf16"], (name, b, h, err)
     # every row keeps its initial norm
     for m in range(3):
+        if W[m] is None:
+            continue
         n_got = torch.linalg.vector_norm(W[m].double(), dim=-1).cpu().numpy()
         n_0 = np.linalg.norm(W0[m].astype(np.float64), axis=-1)
         np.testing.assert_allclose(n_got, np.broadcast_to(n_0, n_got.shape), rtol=1e-5)

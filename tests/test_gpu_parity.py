@@ -37,6 +37,9 @@ SMALL = {
     5: dict(n_kv=8192 + 77, n_q=500),
     6: dict(n_kv=2048),                       # the whole tiny momentum workload
     7: dict(n_kv=2 * 2048 + 301),
+    8: dict(n_kv=4096 + 1000),                # one full chunk + a partial one
+    9: dict(n_kv=2048),                       # the whole tiny linear workload
+    10: dict(n_kv=5000 + 13, n_q=333),
 }
 
 
@@ -102,6 +105,44 @@ def test_gradient_at_head_dim_256_spans_several_token_slices():
     _check_gradient(w.with_tokens(2 * 4096 + 77, seed=w.seed + 2100))
 
 
+# ------------------------------------------------ linear fast-weight memory
+@pytest.mark.parametrize("num,n", [(9, 1000 + 37), (10, 4096 + 99), (10, 1), (10, 64 * 37 + 5), (9, 1)])
+def test_linear_chunk_gradient_matches_oracle(num, n):
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[num].with_tokens(n, seed=li.WORKLOADS[num].seed + 2200)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp, max_chunk=n)
+    k, v, e = to_device(inp.k), to_device(inp.v), to_device(inp.eta)
+    g = torch.empty(w.B, w.H, w.d, w.d, device="cuda")
+    L.lact_chunk_gradient(layer.handle, k, v, e, n, g, None, None)
+    got = to_host_f64(g)
+    for b in range(w.B):
+        for h in range(w.H):
+            want = O.linear_chunk_gradient(inp.W1[h].astype(np.float64), li.as_f64(inp.k[b, h]),
+                                           li.as_f64(inp.v[b, h]), inp.eta[b, h].astype(np.float64))
+            err = rel_l2(got[b, h], want)
+            assert err < TOL[w.dtype], (b, h, err)
+
+
+@pytest.mark.parametrize("num,n_q", [(9, 2048), (10, 333), (10, 1), (10, 128 * 5)])
+def test_linear_apply_matches_oracle(num, n_q):
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[num].with_tokens(128, n_q=n_q, seed=li.WORKLOADS[num].seed + 2300)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    q = to_device(inp.q)
+    o = torch.empty_like(q)
+    L.lact_chunk_apply(layer.handle, q, w.n_q, o)
+    got = to_host_f64(o)
+    for b in range(w.B):
+        for h in range(w.H):
+            want = O.linear_apply(inp.W1[h].astype(np.float64), li.as_f64(inp.q[b, h]))
+            err = rel_l2(got[b, h], want)
+            assert err < TOL[w.dtype], (b, h, err)
+
+
 # ------------------------------------------- rows a5-a7: optimiser + renorm
 @pytest.mark.parametrize("num,opt", [(1, "gd"), (3, "muon"), (4, "muon"), (2, "gd")])
 def test_apply_gradient_matches_oracle(num, opt):
@@ -160,7 +201,7 @@ def test_momentum_velocity_carries_across_two_steps(num):
 
 
 # ------------------------------------------------- whole layer calls (a8)
-@pytest.mark.parametrize("num", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("num", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
 def test_sequence_matches_oracle(num):
     w = _small(num)
     inp = li.make_inputs(w)
@@ -211,11 +252,12 @@ def test_update_beyond_max_chunk_is_rejected():
     assert ex.value.status == L.LACT_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("num", [3, 2, 6, 7])
+@pytest.mark.parametrize("num", [3, 2, 6, 7, 9, 10])
 def test_checkpoint_resume_equals_one_run(num):
     torch = _torch()
     from chunk_test_step_b300 import lact as L
-    w = li.WORKLOADS[num].with_tokens(1024, chunk=256)
+    # (the set-mode workloads' shapes run here in the causal order)
+    w = li.WORKLOADS[num].with_tokens(1024, n_q=1024, chunk=256)
     inp = li.make_inputs(w)
     q, k, v, e = (to_device(x) for x in (inp.q, inp.k, inp.v, inp.eta))
     one = _layer(w, inp)
@@ -235,7 +277,7 @@ def test_checkpoint_resume_equals_one_run(num):
     torch.cuda.synchronize()
     assert torch.equal(torch.cat([o_a, o_b], dim=2), o_one)
     for x, y in zip(W_one, W_two):
-        assert torch.equal(x, y)
+        assert (x is None and y is None) or torch.equal(x, y)
 
 
 def test_nonfinite_row_sets_status():
@@ -269,7 +311,7 @@ def test_profiling_counts_phases():
     assert all(prof[p]["ms"] > 0 for p in prof)
 
 
-@pytest.mark.parametrize("num", [2, 4, 5, 7])
+@pytest.mark.parametrize("num", [2, 4, 5, 7, 8, 10])
 def test_bf16_workloads_run_on_tensor_core_kernels(num):
     # every launch of the readout and gradient phases of the bf16 layers is a
     # tcgen05 kernel (no CUDA-core stand-in)

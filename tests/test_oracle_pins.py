@@ -311,3 +311,56 @@ def test_momentum_first_chunk_equals_gradient_descent():
     _, W_g = O.sequence_causal(W, K, K, V, eta, 5, "gd")
     for a, b in zip(W_m, W_g):
         np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------- linear fast-weight memory
+def test_linear_gradient_matches_central_differences():
+    g = np.random.default_rng(31)
+    d, n = 5, 9
+    W = g.normal(size=(d, d)) / math.sqrt(d)
+    K, V = g.normal(size=(n, d)), g.normal(size=(n, d))
+    eta = 0.02 + 0.01 * g.random(n)
+    G = O.linear_chunk_gradient(W, K, V, eta)
+    h = 1e-6
+    for i in range(d):
+        for j in range(d):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[i, j] += h
+            Wm[i, j] -= h
+            fd = (O.linear_chunk_loss(Wp, K, V, eta) - O.linear_chunk_loss(Wm, K, V, eta)) / (2 * h)
+            assert abs(G[i, j] - fd) < 1e-8 * max(1.0, abs(fd))
+
+
+def test_linear_readout_special_cases():
+    g = np.random.default_rng(32)
+    X = g.normal(size=(6, 4))
+    np.testing.assert_array_equal(O.linear_apply(np.eye(4), X), X)
+    P = np.eye(4)[[2, 0, 3, 1]]          # row i of P picks coordinate perm[i]
+    np.testing.assert_array_equal(O.linear_apply(P, X), X[:, [2, 0, 3, 1]])
+
+
+def test_linear_single_token_step_is_rank_one():
+    # one token: the GD step -dL/dW is eta v k^T, a rank-one matrix
+    g = np.random.default_rng(33)
+    d = 6
+    W = g.normal(size=(d, d))
+    k, v = g.normal(size=(1, d)), g.normal(size=(1, d))
+    step = -O.linear_chunk_gradient(W, k, v, np.array([0.3]))
+    assert np.linalg.matrix_rank(step) == 1
+    np.testing.assert_allclose(step @ k[0], 0.3 * v[0] * (k[0] @ k[0]), rtol=1e-13)
+
+
+def test_linear_causal_and_set_orders():
+    g = np.random.default_rng(34)
+    d, n = 4, 12
+    W = (g.normal(size=(d, d)),)
+    Q, K, V = g.normal(size=(n, d)), g.normal(size=(n, d)), g.normal(size=(n, d))
+    eta = 0.05 * np.ones(n)
+    # causal, one chunk: the readout sees the initial weights
+    o, _ = O.sequence_causal(W, Q, K, V, eta, n, "gd")
+    np.testing.assert_array_equal(o, O.linear_apply(W[0], Q))
+    # set: one step on all tokens, then the read with the new weights
+    o2, W2 = O.sequence_set(W, Q, K, V, eta, "gd")
+    W_exp = O.renorm_update(W[0], -O.linear_chunk_gradient(W[0], K, V, eta))
+    np.testing.assert_allclose(W2[0], W_exp, rtol=1e-14)
+    np.testing.assert_allclose(o2, Q @ W_exp.T, rtol=1e-13)
