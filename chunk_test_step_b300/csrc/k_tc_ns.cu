@@ -19,10 +19,11 @@
 // iteration leaves the chip. After each update a CTA writes its new bf16
 // columns (two 16 KB atoms, contiguous) into its own Xb and pushes them with
 // one bulk copy into the Xb of every other CTA of the cluster (distributed
-// shared memory), completing on that CTA's mbarrier. Two cluster-wide
-// handshakes per iteration order this: "every CTA's A GEMM has finished
-// reading Xb" before anyone overwrites it, and "every CTA's columns have
-// landed" before the next A GEMM.
+// shared memory), completing on that CTA's mbarrier for this source. The next
+// A GEMM starts on the CTA's own columns and takes each other CTA's columns
+// as they land (own block first, then the others in rank order). A
+// cluster-wide handshake, "every CTA's A GEMM has finished reading Xb",
+// comes before anyone overwrites it.
 //
 // 256 threads: thread = row of X (TMEM lane) and half of the CTA's columns;
 // thread 0 also issues the MMAs. Every mbarrier wait is bounded and its
@@ -75,7 +76,8 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
 __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t mbar, sync_a, sync_x;
+    __shared__ __align__(8) uint64_t mbar, sync_a, sync_x[NMAX / CB];
+    __shared__ int fail_sh;
     __shared__ uint32_t tmem_slot;
     __shared__ float red[NTHREADS / 32];
     __shared__ float norm_part[NMAX / CB];   // partial sums of squares, one per CTA of the cluster
@@ -90,13 +92,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     float* G = a.g[which] + (size_t)bh * a.d * a.dh;
     const uint32_t base = smem_u32(sm);
     const uint32_t bar = smem_u32(&mbar);
-    const uint32_t bar_a = smem_u32(&sync_a), bar_x = smem_u32(&sync_x);
+    const uint32_t bar_a = smem_u32(&sync_a);
+    auto barx = [&](int r) { return smem_u32(&sync_x[r]); };   // columns arriving from CTA r
     const int c0 = (int)rank * CB;                 // first column owned by this CTA
 
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(bar_a, cs);   // one arrive per CTA of the cluster
-        mbar_init(bar_x, 1);    // own arrive + the bytes of the other CTAs' columns
+        for (int r = 0; r < cs; ++r) mbar_init(barx(r), 1);   // own expect_tx + CTA r's bytes
+        fail_sh = 0;
         fence_mbar_init();
     }
     // barrier initialisation visible to the whole cluster before any remote arrive
@@ -174,22 +178,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     tc_fence_after();
     const uint32_t xblock = base + OFF_X + (uint32_t)(c0 / 64) * ATOM;   // this CTA's columns of Xb
     constexpr uint32_t XBLOCK_BYTES = 2 * ATOM;
-    // Own columns of Xb out to the other CTAs, theirs in; the bytes are
-    // counted on bar_x. Phase 0 of bar_a and bar_x belong to the set-up, so
-    // iteration `it` uses phase it + 1.
-    auto exchange_columns = [&](uint32_t parity, bool send) -> bool {
+    // Own columns of Xb out to the other CTAs; the bytes from CTA r are
+    // counted on barx(r). Send n (n = 0 at set-up, then after iteration n-1)
+    // is consumed by the A GEMM of iteration n, with parity n & 1.
+    int sends = 0;                 // sends made (thread 0's count)
+    int waited[NMAX / CB] = {0, 0, 0, 0};
+    auto send_columns = [&](bool send) {
         if (tid == 0) {
-            mbar_expect_tx(bar_x, (uint32_t)(cs - 1) * XBLOCK_BYTES);
+            for (int r = 0; r < cs; ++r)
+                if (r != (int)rank) mbar_expect_tx(barx(r), XBLOCK_BYTES);
             if (send)
                 for (int r = 0; r < cs; ++r)
                     if (r != (int)rank)
                         bulk_copy_to_cluster(mapa_shared(xblock, (uint32_t)r), xblock, XBLOCK_BYTES,
-                                             mapa_shared(bar_x, (uint32_t)r));
+                                             mapa_shared(barx((int)rank), (uint32_t)r));
+            ++sends;
         }
-        return __syncthreads_and(mbar_wait_cluster(bar_x, parity, WAIT_NS) ? 1 : 0) != 0;
     };
-    if (!exchange_columns(0, ok)) ok = false;
-    tc_fence_after();
+    send_columns(ok);
 
     uint32_t phase = 0;
     // Wait for the MMAs just committed; the outcome is made block-uniform so
@@ -226,15 +232,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     const uint64_t dAmn = sdesc_sw128(base + OFF_A, ATOM, 1024);  // Ab MN-major
     const uint64_t dB = sdesc_sw128(base + OFF_B, 16, 1024);      // Bb K-major
     for (int it = 0; it < a.steps; ++it) {
-        // A = Xb Xb^T
+        // A = Xb Xb^T: own columns first, then each other CTA's as they land
         if (ok && tid == 0) {
-            for (int j = 0; j < n / 16; ++j) {
-                const uint64_t ko = (uint64_t)((j >> 2) * ATOM + (j & 3) * 32) >> 4;
-                mma_bf16(tmem + COL_A, dX + ko, dX + ko, i_xx, j > 0 ? 1u : 0u);
+            int issued = 0;
+            auto issue_block = [&](int blk) {
+                for (int j = blk * (CB / 16); j < (blk + 1) * (CB / 16); ++j) {
+                    const uint64_t ko = (uint64_t)((j >> 2) * ATOM + (j & 3) * 32) >> 4;
+                    mma_bf16(tmem + COL_A, dX + ko, dX + ko, i_xx, issued++ > 0 ? 1u : 0u);
+                }
+            };
+            issue_block((int)rank);
+            for (int r = 0; r < cs; ++r) {
+                if (r == (int)rank) continue;
+                if (!mbar_wait_cluster(barx(r), (uint32_t)(it & 1), WAIT_NS)) { fail_sh = 1; break; }
+                ++waited[r];
+                tc_fence_after();
+                issue_block(r);
             }
             mma_commit(bar);
         }
         if (ok && !mma_done()) ok = false;
+        if (fail_sh) ok = false;   // read after mma_done's barrier: the same in every thread
         // this CTA's last read of the other CTAs' columns of Xb in the iteration is over
         arrive_a_done();
         if (ok) {
@@ -328,8 +346,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (!exchange_columns((it + 1) & 1, ok)) ok = false;
         tc_fence_after();
+        // (after the last iteration each CTA writes back only its own columns)
+        if (it + 1 < a.steps) send_columns(ok);
     }
     if (!ok) {
         if (tid == 0) atomicOr(a.status, ST_TIMEOUT);
@@ -354,10 +373,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
             }
         }
     }
-    // every MMA has completed once this commit lands (bounded drain)
+    // every MMA has completed once this commit lands (bounded drain); after
+    // an early exit from the loop, columns still on their way in are waited
+    // for (bounded) before the CTA may leave
     if (tid == 0) {
         mma_commit(bar);
         mbar_wait(bar, phase & 1, WAIT_NS);
+        for (int r = 0; r < cs; ++r)
+            if (r != (int)rank)
+                for (int n = waited[r]; n < sends; ++n) mbar_wait_cluster(barx(r), (uint32_t)(n & 1), WAIT_NS);
     }
     tc_fence_before();
     __syncthreads();
