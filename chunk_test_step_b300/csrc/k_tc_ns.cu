@@ -12,10 +12,12 @@
 //     B  = b A + c AA          fp32, from the unrounded A
 //     BX = Bb Xb               Bb = bf16(B) K-major; Xb read MN-major     (TMEM)
 //     X  = a X + BX            fp32
-// The cluster has n/128 CTAs; CTA j owns columns [128 j, 128 j + 128) of X.
-// Every CTA holds the whole bf16 Xb in shared memory (the operand of A) and
-// forms A, AA and B itself (they are small: 128 x 128); it forms only its own
-// 128 columns of BX and keeps its fp32 columns of X in TMEM, so nothing of the
+// The cluster has n/cb CTAs (cb = 256 columns each when n is a multiple of
+// 256, else 128); CTA j owns columns [cb j, cb j + cb) of X. Every CTA holds
+// the whole bf16 Xb in shared memory (the operand of A) and forms A, AA and B
+// itself (they are small: 128 x 128); it forms only its own cb columns of BX
+// and keeps its fp32 columns of X in TMEM (BX reuses the columns of A and AA,
+// which are dead once B is in shared memory), so nothing of the
 // iteration leaves the chip. After each update a CTA writes its new bf16
 // columns (two 16 KB atoms, contiguous) into its own Xb and pushes them with
 // one bulk copy into the Xb of every other CTA of the cluster (distributed
@@ -40,16 +42,19 @@ using namespace tc;
 
 constexpr int M = 128;
 constexpr int NMAX = 512;
-constexpr int CB = 128;                            // columns of X per CTA
+constexpr int MAXCS = 4;                           // CTAs per cluster, at most (n = 512 in 128-column blocks)
 constexpr int NTHREADS = 256;
 constexpr uint32_t ATOM = M * 128;                 // [128 rows][64 bf16] = 16 KB
 constexpr uint32_t OFF_X = 0;                      // n/64 atoms of Xb
 constexpr uint32_t OFF_A = (NMAX / 64) * ATOM;     // 2 atoms of Ab
 constexpr uint32_t OFF_B = OFF_A + 2 * ATOM;       // 2 atoms of Bb
-constexpr int SROW = CB + 1;                       // fp32 staging row stride (words)
-constexpr uint32_t SMEM_STAGE = M * SROW * 4;      // staging of this CTA's fp32 columns, from OFF_A
-constexpr uint32_t SMEM_BYTES = (OFF_A + SMEM_STAGE > OFF_B + 2 * ATOM ? OFF_A + SMEM_STAGE : OFF_B + 2 * ATOM) + 1024;
-constexpr uint32_t COL_A = 0, COL_AA = 128, COL_BX = 256, COL_X = 384;
+constexpr uint32_t SMEM_BYTES = OFF_B + 2 * ATOM + 1024;
+// TMEM: the CTA's fp32 columns of X at 0 (cb columns); from cb on, A (128)
+// and AA (128), later overwritten by BX (cb).
+constexpr uint32_t COL_X = 0;
+
+// Columns of X per CTA for a long side n.
+__host__ __device__ constexpr int ns_block(int n) { return n % 256 == 0 ? 256 : 128; }
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 struct NsArgs {
@@ -76,15 +81,17 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
 __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t mbar, sync_a, sync_x[NMAX / CB];
+    __shared__ __align__(8) uint64_t mbar, sync_a, sync_x[MAXCS];
     __shared__ int fail_sh;
     __shared__ uint32_t tmem_slot;
     __shared__ float red[NTHREADS / 32];
-    __shared__ float norm_part[NMAX / CB];   // partial sums of squares, one per CTA of the cluster
+    __shared__ float norm_part[MAXCS];   // partial sums of squares, one per CTA of the cluster
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = a.n;
-    const int cs = n / CB;                         // CTAs in the cluster
+    const int cb = ns_block(n);                    // columns of X per CTA
+    const int cs = n / cb;                         // CTAs in the cluster
+    const uint32_t COL_A = (uint32_t)cb, COL_AA = COL_A + 128, COL_BX = COL_A;
     const uint32_t rank = cluster_rank();
     const int mi = blockIdx.x / cs, which = mi / a.BH, bh = mi % a.BH;
     const int rows = which == 1 ? a.d : a.dh, cols = which == 1 ? a.dh : a.d;
@@ -94,7 +101,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     const uint32_t bar = smem_u32(&mbar);
     const uint32_t bar_a = smem_u32(&sync_a);
     auto barx = [&](int r) { return smem_u32(&sync_x[r]); };   // columns arriving from CTA r
-    const int c0 = (int)rank * CB;                 // first column owned by this CTA
+    const int c0 = (int)rank * cb;                 // first column owned by this CTA
 
     if (tid == 0) {
         mbar_init(bar, 1);
@@ -110,32 +117,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         tmem_alloc(smem_u32(&tmem_slot), 512);
         tmem_relinquish();
     }
-    // ---- X = G / (||G||_F + eps). Each CTA reads only its own columns of X
-    // (a quarter of G for n = 512) into fp32 staging (rows padded to 129
-    // floats, so a warp's 32 rows fall in 32 banks), sums their squares, and
-    // posts the partial sum to every CTA of the cluster; every CTA adds the
-    // partials in rank order, so all hold the same norm.
+    // ---- X = G / (||G||_F + eps). Each CTA reads its own columns of X twice:
+    // first for their sum of squares, posted to every CTA of the cluster
+    // (every CTA adds the partials in rank order, so all hold the same norm),
+    // then for the values, fp32 into TMEM and bf16 into its block of Xb.
+    // Thread (row, half) owns row `row` of X and hc = cb/2 of the columns.
     const int q = warp & 3, half = warp >> 2;
     const int row = 32 * q + lane;             // row of X owned by this thread
-    float* stage = reinterpret_cast<float*>(sm + OFF_A);   // [128 rows][SROW] fp32
-    const float4* G4 = reinterpret_cast<const float4*>(G);
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 16
-    for (int i = tid; i < M * CB / 4; i += NTHREADS) {
-        // four consecutive elements of G: X[gc + t][gr] when G is stored tall
-        // (its rows are columns of X), else X[gr][gc + t]
-        const int gr = tr ? c0 + (4 * i) / M : (4 * i) / CB;
-        const int gc = tr ? (4 * i) % M : c0 + (4 * i) % CB;
-        const float4 v = G4[((size_t)gr * cols + gc) / 4];
-        s4[i & 3] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, s4[i & 3]))));
-        const float x[4] = {v.x, v.y, v.z, v.w};
+    const int hc = cb / 2;
+    // 32 consecutive columns j0.. of this thread's row: element (row, j) of X
+    // is G[j][row] when G is stored tall (a warp's 32 rows read 32
+    // consecutive words), else G[row][j] (the thread reads 128 contiguous bytes)
+    auto load32 = [&](int j0, float* x) {
+        if (tr) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int xr = tr ? gc + t : gr, xc = tr ? gr : gc + t;
-            stage[xr * SROW + (xc - c0)] = x[t];
+            for (int t = 0; t < 32; ++t) x[t] = G[(size_t)(j0 + t) * cols + row];
+        } else {
+            const float4* gp = reinterpret_cast<const float4*>(G + (size_t)row * cols + j0);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const float4 v = gp[t];
+                x[4 * t] = v.x; x[4 * t + 1] = v.y; x[4 * t + 2] = v.z; x[4 * t + 3] = v.w;
+            }
         }
+    };
+    float ss = 0.f;
+    for (int h = 0; h < hc / 32; ++h) {
+        float x[32];
+        load32(c0 + half * hc + h * 32, x);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) ss = fmaf(x[t], x[t], ss);
     }
-    float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) red[warp] = ss;
     tc_fence_before();
@@ -155,15 +167,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     float tot = 0.f;
     for (int r = 0; r < cs; ++r) tot += norm_part[r];
     const float nrm = sqrtf(tot) + 1e-7f;
-    // this CTA's columns: fp32 into TMEM, bf16 into its block of Xb
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t v[32];
+    for (int h = 0; h < hc / 32; ++h) {
+        const int j0 = half * hc + h * 32;       // within this CTA's columns
         float xv[32];
-        const int j0 = half * 64 + h * 32;
+        uint32_t v[32];
+        load32(c0 + j0, xv);
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
-            xv[t] = stage[row * SROW + j0 + t] / nrm;
+            xv[t] = xv[t] / nrm;
             v[t] = __float_as_uint(xv[t]);
         }
         tmem_st32(lane_base + COL_X + j0, v);
@@ -177,12 +188,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t xblock = base + OFF_X + (uint32_t)(c0 / 64) * ATOM;   // this CTA's columns of Xb
-    constexpr uint32_t XBLOCK_BYTES = 2 * ATOM;
+    const uint32_t XBLOCK_BYTES = (uint32_t)(cb / 64) * ATOM;
     // Own columns of Xb out to the other CTAs; the bytes from CTA r are
     // counted on barx(r). Send n (n = 0 at set-up, then after iteration n-1)
     // is consumed by the A GEMM of iteration n, with parity n & 1.
     int sends = 0;                 // sends made (thread 0's count)
-    int waited[NMAX / CB] = {0, 0, 0, 0};
+    int waited[MAXCS] = {0, 0, 0, 0};
     auto send_columns = [&](bool send) {
         if (tid == 0) {
             for (int r = 0; r < cs; ++r)
@@ -225,7 +236,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     };
     const uint32_t i_xx = idesc_bf16_f32(M, M, 0, 0);
     const uint32_t i_aa = idesc_bf16_f32(M, M, 0, 1);
-    const uint32_t i_bx = idesc_bf16_f32(M, CB, 0, 1);
+    const uint32_t i_bx = idesc_bf16_f32(M, cb, 0, 1);
     const uint64_t dX = sdesc_sw128(base + OFF_X, 16, 1024);      // Xb K-major
     const uint64_t dXmn = sdesc_sw128(base + OFF_X, ATOM, 1024);  // Xb MN-major
     const uint64_t dA = sdesc_sw128(base + OFF_A, 16, 1024);      // Ab K-major
@@ -236,7 +247,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         if (ok && tid == 0) {
             int issued = 0;
             auto issue_block = [&](int blk) {
-                for (int j = blk * (CB / 16); j < (blk + 1) * (CB / 16); ++j) {
+                for (int j = blk * (cb / 16); j < (blk + 1) * (cb / 16); ++j) {
                     const uint64_t ko = (uint64_t)((j >> 2) * ATOM + (j & 3) * 32) >> 4;
                     mma_bf16(tmem + COL_A, dX + ko, dX + ko, i_xx, issued++ > 0 ? 1u : 0u);
                 }
@@ -305,7 +316,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
                 }
             }
             sync_smem();
-            // BX_j = Bb Xb[:, c0 : c0 + 128]
+            // BX_j = Bb Xb[:, c0 : c0 + cb] (over the dead A and AA)
             if (tid == 0) {
                 const uint64_t xo = (uint64_t)((c0 / 64) * ATOM) >> 4;
 #pragma unroll
@@ -320,10 +331,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         // no CTA still reads Xb with its A GEMM
         if (!cluster_wait(bar_a, (it + 1) & 1)) ok = false;
         if (ok) {
-            // X_j = a X_j + BX_j in TMEM; bf16(X_j) into Xb of every CTA
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int j0 = half * 64 + h * 32;
+            // X_j = a X_j + BX_j in TMEM; bf16(X_j) into this CTA's block of Xb
+            for (int h = 0; h < hc / 32; ++h) {
+                const int j0 = half * hc + h * 32;
                 uint32_t vx[32], vb[32];
                 tmem_ld32(lane_base + COL_X + j0, vx);
                 tmem_ld32(lane_base + COL_BX + j0, vb);
@@ -354,9 +364,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         if (tid == 0) atomicOr(a.status, ST_TIMEOUT);
     } else {
         // this CTA's columns back into G's own orientation
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int j0 = half * 64 + h * 32;
+        for (int h = 0; h < hc / 32; ++h) {
+            const int j0 = half * hc + h * 32;
             uint32_t v[32];
             tmem_ld32(lane_base + COL_X + j0, v);
             tmem_wait_ld();
@@ -399,7 +408,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
 bool ns_tc_supported(const lact_state* st) {
     const int m = st->cfg.d < st->cfg.dh ? st->cfg.d : st->cfg.dh;
     const int n = st->cfg.d < st->cfg.dh ? st->cfg.dh : st->cfg.d;
-    return st->cfg.io_dtype == LACT_BF16 && m == M && n <= NMAX && n % CB == 0;
+    return st->cfg.io_dtype == LACT_BF16 && m == M && n <= NMAX && n % 128 == 0;
 }
 
 cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s) {
@@ -416,7 +425,7 @@ cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s)
     a.status = st->status;
     cudaError_t e = cudaFuncSetAttribute(k_ns_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int cs = a.n / CB;
+    const int cs = a.n / ns_block(a.n);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)(cs * st->nmat * st->BH));
     lc.blockDim = dim3(NTHREADS);
