@@ -249,8 +249,16 @@ lact_status lact_init_state(lact_state** out, const lact_config* cfg, void* d_ws
     st->profiling = false;
     memset(&st->prof, 0, sizeof(st->prof));
     int dev = 0;
+    st->side = nullptr;
+    st->ev_fork = st->ev_join = nullptr;
     if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&st->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&st->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&st->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&st->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&st->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+        if (st->ev_fork) cudaEventDestroy(st->ev_fork);
+        if (st->ev_join) cudaEventDestroy(st->ev_join);
+        if (st->side) cudaStreamDestroy(st->side);
         delete st;
         return LACT_ERR_CUDA;
     }
@@ -266,6 +274,9 @@ lact_status lact_init_state(lact_state** out, const lact_config* cfg, void* d_ws
                                st->f64, (size_t)cfg->H * per_head, st->num_sms, s);
     if (e == cudaSuccess) e = launch_shadow(st, s);
     if (e != cudaSuccess) {
+        cudaEventDestroy(st->ev_fork);
+        cudaEventDestroy(st->ev_join);
+        cudaStreamDestroy(st->side);
         delete st;
         return LACT_ERR_CUDA;
     }
@@ -349,12 +360,19 @@ lact_status lact_sequence(lact_state* st, lact_order order, const void* d_q, int
     st->last_stream = s;
     if (order == LACT_CAUSAL_APPLY_THEN_UPDATE) {
         if (n_q != n_kv) return LACT_ERR_INVALID_ARG;
+        // The readout of a chunk and its gradient both read W_c and nothing
+        // else of each other: the readout runs on the side stream beside the
+        // gradient, and the two join before the update changes W.
         for (int64_t t0 = 0; t0 < n_kv; t0 += chunk) {
             const int64_t n = n_kv - t0 < chunk ? n_kv - t0 : chunk;
-            r = do_apply(st, TokView{d_q, n_q, t0, n}, d_o, s);
+            if (cudaEventRecord(st->ev_fork, s) != cudaSuccess || cudaStreamWaitEvent(st->side, st->ev_fork, 0) != cudaSuccess)
+                return LACT_ERR_CUDA;
+            r = do_apply(st, TokView{d_q, n_q, t0, n}, d_o, st->side);
             if (r != LACT_OK) return r;
+            if (cudaEventRecord(st->ev_join, st->side) != cudaSuccess) return LACT_ERR_CUDA;
             r = do_grad(st, TokView{d_k, n_kv, t0, n}, TokView{d_v, n_kv, t0, n}, d_eta, false, st->dW, s);
             if (r != LACT_OK) return r;
+            if (cudaStreamWaitEvent(s, st->ev_join, 0) != cudaSuccess) return LACT_ERR_CUDA;
             r = do_step(st, st->dW, s);
             if (r != LACT_OK) return r;
         }
@@ -466,6 +484,10 @@ const char* lact_status_str(lact_status s) {
 void lact_free_state(lact_state* st) {
     if (!st) return;
     drain_profile(st);
+    cudaStreamSynchronize(st->side);
+    cudaEventDestroy(st->ev_fork);
+    cudaEventDestroy(st->ev_join);
+    cudaStreamDestroy(st->side);
     for (cudaEvent_t e : st->event_pool) cudaEventDestroy(e);
     delete st;
 }

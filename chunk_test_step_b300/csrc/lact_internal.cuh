@@ -63,6 +63,8 @@ struct lact_state {
     int64_t slice_cap;
     int* status;
     cudaStream_t last_stream;
+    cudaStream_t side;        // causal order: each chunk's readout runs here, beside its gradient
+    cudaEvent_t ev_fork, ev_join;
     bool profiling;
     std::vector<lact::PhaseEvents> pending;
     std::vector<cudaEvent_t> event_pool;

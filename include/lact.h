@@ -131,6 +131,8 @@ lact_status lact_chunk_update(lact_state* st, const void* d_k, const void* d_v,
  * LACT_CAUSAL_APPLY_THEN_UPDATE: q and k/v are the same n = n_q = n_kv
  *   tokens, cut into chunks of `chunk` (the last may be shorter); each chunk
  *   is first read with the current W (into d_o), then W is updated on it.
+ *   (A chunk's readout runs on a stream of the state's own, joined back into
+ *   `stream` before the update; everything is complete in `stream` order.)
  * LACT_SET_UPDATE_THEN_APPLY: all n_kv input tokens form one update; they
  *   are taken in slices of `chunk` whose gradients are summed before a single
  *   optimiser step; then the n_q queries are read.
