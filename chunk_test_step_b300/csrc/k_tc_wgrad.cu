@@ -11,8 +11,9 @@
 // Each is C (+)= A^T B summed over the tokens, with A and B stored
 // token-major (row = token), so both are MN-major operands. One CTA computes
 // a 128 x NB tile of one product for one head over the tokens of its split
-// (one split here: no partial sums), with a 4-deep TMA pipeline of 64-token
-// stages and the fp32 accumulator in TMEM.
+// (one split here: no partial sums), with a TMA pipeline of 64-token stages
+// (4 deep at NB = 256, 6 at NB = 128, in the same 192 KB) and the fp32
+// accumulator in TMEM.
 //
 // The same kernel forms the chunk gradient of the linear fast-weight memory,
 // dW = -(eta V)^T K (LaCT review page, Fig. 8: the linear state): there the
@@ -35,16 +36,16 @@ using namespace tc;
 
 constexpr int TM = 128;        // rows of C per CTA
 constexpr int TK = 64;         // tokens per stage
-constexpr int STAGES = 4;
+constexpr int MAXST = 6;       // stages, at most
 constexpr int NBMAX = 256;     // columns of C per CTA (at most)
 constexpr int NTHREADS = 192;
 constexpr uint32_t BOXB = TK * 128;                       // one [64 tokens][64 elements] box: 8 KB
 constexpr uint32_t A_BYTES = (TM / 64) * BOXB;            // 16 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + (NBMAX / 64) * BOXB;   // 48 KB
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr uint32_t RING_BYTES = 4 * (A_BYTES + (NBMAX / 64) * BOXB);   // 192 KB: 4 stages at NB = 256
+constexpr uint32_t SMEM_BYTES = RING_BYTES + 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-enum { B_F = 0, B_E = STAGES, B_S = 2 * STAGES, B_ACC = 3 * STAGES, B_DRAIN, NBARS };
+enum { B_F = 0, B_E = MAXST, B_S = 2 * MAXST, B_ACC = 3 * MAXST, B_DRAIN, NBARS };
 
 // One product C (+)= A^T B of one head. The tensor maps cover all heads:
 // A: (ma inner, tokens, heads), B: (nb inner, tokens, heads).
@@ -94,13 +95,15 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
     const int tok1 = min(a.ntok, tok0 + a.toks_per_split);
     const int nsteps = tok1 > tok0 ? (tok1 - tok0 + TK - 1) / TK : 0;
     const bool scale = a.eta != nullptr;
+    const uint32_t STAGE_BYTES = A_BYTES + (uint32_t)(NB / 64) * BOXB;
+    const int STAGES = min(MAXST, (int)(RING_BYTES / STAGE_BYTES));
     const uint32_t base = smem_u32(sm);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     if (tid == 0) {
         skip_cta = (*reinterpret_cast<volatile int*>(a.status) & ST_TIMEOUT) ? 1 : 0;
         abort_flag = 0;
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < MAXST; ++s) {
             mbar_init(bar(B_F + s), 1);
             mbar_init(bar(B_E + s), 1);
             mbar_init(bar(B_S + s), 4);
@@ -130,7 +133,7 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
         if (lane == 0) {
             prefetch_tmap(tma);
             prefetch_tmap(tmb);
-            const uint32_t bytes = A_BYTES + (uint32_t)(NB / 64) * BOXB;
+            const uint32_t bytes = STAGE_BYTES;
             int issued = 0;
             for (int i = 0; i < nsteps && !*abort_v; ++i) {
                 const int s = i % STAGES;
@@ -177,11 +180,18 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
             const int et = tid - 64;                    // 0..127: (64-element block, token row)
             const int blk = et >> 6, trow = et & 63;
             const float* eh = a.eta + (int64_t)h * a.eta_n_total + a.eta_t0;
+            // eta of this thread's row, fetched one stage ahead so its DRAM
+            // latency overlaps the stage's TMA
+            auto eta_row = [&](int i) -> float {
+                const int tok = tok0 + i * TK + trow;
+                return (i < nsteps && tok < tok1) ? -eh[tok] : 0.0f;
+            };
+            float ne_next = eta_row(0);
             for (int i = 0; i < nsteps; ++i) {
                 const int s = i % STAGES;
+                const float ne = ne_next;
+                ne_next = eta_row(i + 1);
                 if (*abort_v || !mbar_wait_warp(bar(B_F + s), (i / STAGES) & 1, WAIT_NS)) { give_up(); break; }
-                const int tok = tok0 + i * TK + trow;
-                const float ne = tok < tok1 ? -eh[tok] : 0.0f;
                 uint4* rp = reinterpret_cast<uint4*>(sm + s * STAGE_BYTES + blk * BOXB + trow * 128);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
