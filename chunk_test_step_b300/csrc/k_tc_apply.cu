@@ -5,8 +5,9 @@
 // read the adapted weights; "Local attention and nonlinear memory work
 // together": the three-matrix SwiGLU memory).
 //
-// One CTA per (head, 128-query tile). The hidden units are visited in blocks
-// r of 64:
+// One CTA per (head, 128-query tile); the launcher uses this kernel at head
+// dim 256 and k_apply2_tc (k_tc_apply2.cu: two query tiles per CTA sharing
+// every weight block) at 128. The hidden units are visited in blocks r of 64:
 //   [H1 | H3] (TMEM, double-buffered) = Q . [W1_r ; W3_r]^T   (A, B K-major)
 //   U_r = silu(H1) * H3 -> bf16, swizzled K-major operand       (epilogue)
 //   O (TMEM, D cols) += U_r . W2[:, r]^T                        (A, B K-major)
@@ -335,7 +336,7 @@ static cudaError_t launch_apply_d(const lact_state* st, TokView q, void* o, cuda
 }
 
 cudaError_t launch_apply_tc(const lact_state* st, TokView q, void* o, cudaStream_t s) {
-    if (st->cfg.d == 128) return launch_apply_d<128>(st, q, o, s);
+    if (st->cfg.d == 128) return launch_apply2_tc(st, q, o, s);
     return launch_apply_d<256>(st, q, o, s);
 }
 

@@ -138,6 +138,8 @@ bool ns_tc_supported(const lact_state* st);
 cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s);
 bool apply_tc_supported(const lact_state* st);
 cudaError_t launch_apply_tc(const lact_state* st, TokView q, void* o, cudaStream_t s);
+// Head dim 128: two 128-query tiles per CTA sharing every streamed weight block.
+cudaError_t launch_apply2_tc(const lact_state* st, TokView q, void* o, cudaStream_t s);
 // Two-kernel chunk gradient (bf16 io, head dim 256): per-token dh1, dh3, u'
 // of a token slice, then the three weight-gradient GEMMs over the slice.
 bool fwdbwd_tc_supported(const lact_state* st);
