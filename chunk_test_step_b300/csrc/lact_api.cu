@@ -452,6 +452,18 @@ lact_status lact_sync_status(lact_state* st) {
     return LACT_OK;
 }
 
+lact_status lact_clear_status(lact_state* st, cudaStream_t s) {
+    if (!st) return LACT_ERR_INVALID_ARG;
+    st->last_stream = s;
+    return cuda_status(cudaMemsetAsync(st->status, 0, 64 * 4, s));
+}
+
+lact_status lact_selftest_timeout(lact_state* st, int64_t budget_ns, cudaStream_t s) {
+    if (!st || budget_ns < 1 || budget_ns > 10000000000LL) return LACT_ERR_INVALID_ARG;
+    st->last_stream = s;
+    return cuda_status(launch_wait_selftest(st->status, (uint64_t)budget_ns, s));
+}
+
 lact_status lact_set_profiling(lact_state* st, int enable) {
     if (!st) return LACT_ERR_INVALID_ARG;
     drain_profile(st);

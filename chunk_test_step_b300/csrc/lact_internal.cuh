@@ -169,6 +169,8 @@ cudaError_t launch_grad_simt_bf16_raw(int d, int dh, int BH, const float* W1, co
                                       int num_sms, int* slots, cudaStream_t s);
 cudaError_t launch_reduce_f32_raw(const float* partial, int slots, size_t mat, float* o0, float* o1, float* o2,
                                   int num_sms, cudaStream_t s);
+// One thread waits (bounded) on an mbarrier nobody arrives on; sets ST_TIMEOUT.
+cudaError_t launch_wait_selftest(int* status, uint64_t budget_ns, cudaStream_t s);
 // Element conversion between the API's fp32 buffers and internal reals.
 cudaError_t launch_convert(const void* src, bool src_f64, void* dst, bool dst_f64, size_t n, int num_sms,
                            cudaStream_t s);

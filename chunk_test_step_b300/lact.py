@@ -27,7 +27,7 @@ SYMBOLS = ("lact_workspace_bytes", "lact_init_state", "lact_chunk_apply", "lact_
            "lact_sequence", "lact_chunk_gradient", "lact_apply_gradient", "lact_get_weights",
            "lact_set_weights", "lact_state_bytes", "lact_export_state", "lact_import_state",
            "lact_chunk_gradient_noalloc",
-           "lact_sync_status", "lact_set_profiling", "lact_get_profile",
+           "lact_sync_status", "lact_clear_status", "lact_selftest_timeout", "lact_set_profiling", "lact_get_profile",
            "lact_launch_count", "lact_status_str", "lact_free_state")
 
 
@@ -81,6 +81,8 @@ def load() -> ctypes.CDLL:
     lib.lact_chunk_gradient_noalloc.argtypes = [P(lact_config), vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]
     lib.lact_chunk_gradient_noalloc.restype = cint
     lib.lact_sync_status.argtypes = [vp]
+    lib.lact_clear_status.argtypes = [vp, vp]
+    lib.lact_selftest_timeout.argtypes = [vp, i64, vp]
     lib.lact_set_profiling.argtypes = [vp, cint]
     lib.lact_get_profile.argtypes = [vp, P(lact_profile)]
     lib.lact_launch_count.argtypes = []
@@ -92,7 +94,8 @@ def load() -> ctypes.CDLL:
     for name in ("lact_init_state", "lact_chunk_apply", "lact_chunk_update", "lact_sequence",
                  "lact_chunk_gradient", "lact_apply_gradient", "lact_get_weights", "lact_set_weights",
                  "lact_export_state", "lact_import_state",
-                 "lact_sync_status", "lact_set_profiling", "lact_get_profile"):
+                 "lact_sync_status", "lact_clear_status", "lact_selftest_timeout", "lact_set_profiling",
+                 "lact_get_profile"):
         getattr(lib, name).restype = cint
     _lib = lib
     return lib
@@ -199,6 +202,14 @@ def lact_chunk_gradient_noalloc(cfg: lact_config, W1, W2, W3, k, v, eta, n_tok: 
 
 def lact_sync_status(st: int) -> int:
     return int(load().lact_sync_status(st))
+
+
+def lact_clear_status(st: int, stream=None) -> None:
+    _check(load().lact_clear_status(st, _s(stream)), "lact_clear_status")
+
+
+def lact_selftest_timeout(st: int, budget_ns: int, stream=None) -> None:
+    _check(load().lact_selftest_timeout(st, budget_ns, _s(stream)), "lact_selftest_timeout")
 
 
 def lact_set_profiling(st: int, enable: bool) -> None:

@@ -200,6 +200,17 @@ lact_status lact_chunk_gradient_noalloc(const lact_config* cfg, const float* d_W
  * (LACT_OK, LACT_ERR_TIMEOUT or LACT_ERR_NONFINITE), or LACT_ERR_CUDA. */
 lact_status lact_sync_status(lact_state* st);
 
+/* Clear the sticky device status (enqueued on `stream`), e.g. after a caller
+ * has handled LACT_ERR_TIMEOUT or LACT_ERR_NONFINITE; while it is set, the
+ * library's tensor-core kernels skip their work. */
+lact_status lact_clear_status(lact_state* st, cudaStream_t stream);
+
+/* Test hook of the failure path every bounded device-side wait takes: one
+ * thread waits on an mbarrier that nothing arrives on, for budget_ns
+ * nanoseconds (1 .. 1e10), then sets the sticky timeout status and returns;
+ * lact_sync_status then reports LACT_ERR_TIMEOUT. Nothing traps or hangs. */
+lact_status lact_selftest_timeout(lact_state* st, int64_t budget_ns, cudaStream_t stream);
+
 /* Per-phase CUDA-event timing of every later call (on: 1, off: 0; turning it
  * on clears the totals). lact_get_profile synchronises and returns totals. */
 lact_status lact_set_profiling(lact_state* st, int enable);

@@ -327,3 +327,67 @@ def test_bf16_workloads_run_on_tensor_core_kernels(num):
     prof = L.lact_get_profile(layer.handle)
     for ph in ("apply", "grad"):
         assert prof[ph]["launches"] > 0 and prof[ph]["tensor_launches"] == prof[ph]["launches"], (ph, prof[ph])
+
+
+# ------------------------------------------------------ failure detection
+def test_bounded_wait_times_out_and_the_state_recovers():
+    # a device-side wait that nothing satisfies gives up after its budget,
+    # sets the sticky status and returns; after the caller clears it, the
+    # same state computes correctly again
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[2].with_tokens(2048 + 300, seed=li.WORKLOADS[2].seed + 5000)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    L.lact_selftest_timeout(layer.handle, 2_000_000)        # 2 ms
+    assert L.lact_sync_status(layer.handle) == L.LACT_ERR_TIMEOUT
+    L.lact_clear_status(layer.handle)
+    assert L.lact_sync_status(layer.handle) == L.LACT_OK
+    q, k, v, e = (to_device(x) for x in (inp.q, inp.k, inp.v, inp.eta))
+    order = L.LACT_CAUSAL_APPLY_THEN_UPDATE if w.order == "causal" else L.LACT_SET_UPDATE_THEN_APPLY
+    o = layer.sequence(order, q, k, v, e, w.chunk)
+    W = layer.weights()
+    torch.cuda.synchronize()
+    assert L.lact_sync_status(layer.handle) == L.LACT_OK
+    errs = compare(w, tuple(to_host_f64(x) for x in (o, *W)), O.run_workload(w, inp))
+    assert max(errs.values()) < TOL[w.dtype], errs
+
+
+# --------------------------------------------- writes stay inside buffers
+@pytest.mark.parametrize("num", [1, 2, 5, 8, 10])
+def test_kernels_write_only_inside_their_buffers(num):
+    # outputs and the workspace sit between canary regions; after a layer
+    # call and a gradient call every canary byte is unchanged
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = _small(num)
+    inp = li.make_inputs(w)
+    cfg = config_for(w)
+    G = 4096                                                  # guard bytes on each side (256-aligned)
+    canary = 0xA5
+
+    def guarded(nbytes):
+        buf = torch.full((nbytes + 2 * G,), canary, dtype=torch.uint8, device="cuda")
+        return buf, buf[G:G + nbytes]
+
+    ws_buf, ws = guarded(L.lact_workspace_bytes(cfg))
+    st = L.lact_init_state(cfg, ws, *(to_device(x) for x in (inp.W1, inp.W2, inp.W3)))
+    q, k, v, e = (to_device(x) for x in (inp.q, inp.k, inp.v, inp.eta))
+    o_buf, o_bytes = guarded(q.numel() * q.element_size())
+    o = o_bytes.view(q.dtype).view(q.shape)
+    order = L.LACT_CAUSAL_APPLY_THEN_UPDATE if w.order == "causal" else L.LACT_SET_UPDATE_THEN_APPLY
+    L.lact_sequence(st, order, q, w.n_q, k, v, e, w.n_kv, w.chunk, o)
+    n = min(w.n_kv, w.chunk)
+    shapes = ((w.dh, w.d),) if w.memory == "linear" else ((w.dh, w.d), (w.d, w.dh), (w.dh, w.d))
+    gbufs, gs = [], []
+    for sh in shapes:
+        b, g = guarded(w.B * w.H * sh[0] * sh[1] * 4)
+        gbufs.append(b)
+        gs.append(g.view(torch.float32))
+    gs += [None] * (3 - len(gs))
+    L.lact_chunk_gradient(st, k, v, e, n, *gs)
+    torch.cuda.synchronize()
+    assert L.lact_sync_status(st) == L.LACT_OK
+    for buf in [ws_buf, o_buf] + gbufs:
+        assert torch.all(buf[:G] == canary) and torch.all(buf[-G:] == canary)
+    L.lact_free_state(st)
