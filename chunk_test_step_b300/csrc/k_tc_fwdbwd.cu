@@ -101,6 +101,27 @@ __device__ __forceinline__ uint32_t pack_f2(f2 v) {
     return pack_bf16(lo, hi);
 }
 
+__device__ __forceinline__ uint4 shfl_xor_u4(uint4 v, int mask) {
+    return make_uint4(__shfl_xor_sync(0xffffffffu, v.x, mask), __shfl_xor_sync(0xffffffffu, v.y, mask),
+                      __shfl_xor_sync(0xffffffffu, v.z, mask), __shfl_xor_sync(0xffffffffu, v.w, mask));
+}
+
+// 4 x 4 transpose of 16-byte chunks within each quad of lanes. On entry lane
+// 4m + g holds chunks 0..3 of its own row; on exit it holds chunk g of rows
+// 4m .. 4m + 3 (c[k] = row 4m + k). Two exchanges: chunk pairs with the lane
+// two apart, then single chunks with the neighbouring lane.
+__device__ __forceinline__ void quad_transpose(uint4 (&c)[4], int lane) {
+    const bool b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
+    {
+        const uint4 r0 = shfl_xor_u4(b1 ? c[0] : c[2], 2), r1 = shfl_xor_u4(b1 ? c[1] : c[3], 2);
+        if (b1) { c[0] = r0; c[1] = r1; } else { c[2] = r0; c[3] = r1; }
+    }
+    {
+        const uint4 r0 = shfl_xor_u4(b0 ? c[0] : c[1], 1), r1 = shfl_xor_u4(b0 ? c[2] : c[3], 1);
+        if (b0) { c[0] = r0; c[2] = r1; } else { c[1] = r0; c[3] = r1; }
+    }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_fwdbwd_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w3,
@@ -268,16 +289,29 @@ k_fwdbwd_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                 p3[j / 2] = pack_f2(f2_mul(du, si));
                 p1[j / 2] = pack_f2(f2_mul(f2_mul(du, x3), g));
             }
-            if (tok < a.n) {
-                bf16* o1 = a.out + ((size_t)bh * a.slice_cap + tok) * a.dh + r * HB + hf * 32;
-                uint4* d1 = reinterpret_cast<uint4*>(o1);
-                uint4* d3 = reinterpret_cast<uint4*>(o1 + one);
-                uint4* du = reinterpret_cast<uint4*>(o1 + 2 * one);
+            // Each thread holds 64 contiguous bytes of its token's row of each
+            // output. After a transpose within each quad of lanes, four lanes
+            // store one row's 64 bytes together: a warp store covers 8 rows in
+            // whole 32-byte sectors instead of 16 bytes of each of 32 rows.
+            uint4 c1[4], c3[4], cu[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    d1[c] = make_uint4(p1[4 * c], p1[4 * c + 1], p1[4 * c + 2], p1[4 * c + 3]);
-                    d3[c] = make_uint4(p3[4 * c], p3[4 * c + 1], p3[4 * c + 2], p3[4 * c + 3]);
-                    du[c] = make_uint4(pu[4 * c], pu[4 * c + 1], pu[4 * c + 2], pu[4 * c + 3]);
+            for (int c = 0; c < 4; ++c) {
+                c1[c] = make_uint4(p1[4 * c], p1[4 * c + 1], p1[4 * c + 2], p1[4 * c + 3]);
+                c3[c] = make_uint4(p3[4 * c], p3[4 * c + 1], p3[4 * c + 2], p3[4 * c + 3]);
+                cu[c] = make_uint4(pu[4 * c], pu[4 * c + 1], pu[4 * c + 2], pu[4 * c + 3]);
+            }
+            quad_transpose(c1, lane);
+            quad_transpose(c3, lane);
+            quad_transpose(cu, lane);
+            const int64_t quad_tok = tok - (lane & 3);      // token of the quad's row 0
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                if (quad_tok + k4 < a.n) {
+                    bf16* o1 = a.out + ((size_t)bh * a.slice_cap + quad_tok + k4) * a.dh + r * HB + hf * 32 +
+                               8 * (lane & 3);
+                    *reinterpret_cast<uint4*>(o1) = c1[k4];
+                    *reinterpret_cast<uint4*>(o1 + one) = c3[k4];
+                    *reinterpret_cast<uint4*>(o1 + 2 * one) = cu[k4];
                 }
             }
         }
