@@ -19,9 +19,10 @@
 // and keeps its fp32 columns of X in TMEM (BX reuses the columns of A and AA,
 // which are dead once B is in shared memory), so nothing of the
 // iteration leaves the chip. After each update a CTA writes its new bf16
-// columns (two 16 KB atoms, contiguous) into its own Xb and pushes them with
-// one bulk copy into the Xb of every other CTA of the cluster (distributed
-// shared memory), completing on that CTA's mbarrier for this source. The next
+// columns into its own Xb; each half of the CTA (128 threads, whole 16 KB
+// atoms) pushes its columns with one bulk copy into the Xb of every other CTA
+// of the cluster (distributed shared memory) as soon as it has written them,
+// completing on that CTA's mbarrier for this source. The next
 // A GEMM starts on the CTA's own columns and takes each other CTA's columns
 // as they land (own block first, then the others in rank order). A
 // cluster-wide handshake, "every CTA's A GEMM has finished reading Xb",
@@ -117,10 +118,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         tmem_alloc(smem_u32(&tmem_slot), 512);
         tmem_relinquish();
     }
-    // ---- X = G / (||G||_F + eps). Each CTA reads its own columns of X twice:
-    // first for their sum of squares, posted to every CTA of the cluster
-    // (every CTA adds the partials in rank order, so all hold the same norm),
-    // then for the values, fp32 into TMEM and bf16 into its block of Xb.
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    // ---- X = G / (||G||_F + eps). Each CTA reads its own columns of G once,
+    // into TMEM as fp32, summing their squares; the partial sum is posted to
+    // every CTA of the cluster (every CTA adds the partials in rank order, so
+    // all hold the same norm). Then each thread scales its values in TMEM and
+    // writes them as bf16 into its block of Xb.
     // Thread (row, half) owns row `row` of X and hc = cb/2 of the columns.
     const int q = warp & 3, half = warp >> 2;
     const int row = 32 * q + lane;             // row of X owned by this thread
@@ -141,20 +147,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
             }
         }
     };
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
     float ss = 0.f;
-    for (int h = 0; h < hc / 32; ++h) {
-        float x[32];
-        load32(c0 + half * hc + h * 32, x);
+    for (int h = 0; h < hc / 32; h += 2) {
+        // two 32-column pieces in flight at once
+        float x0[32], x1[32];
+        load32(c0 + half * hc + h * 32, x0);
+        load32(c0 + half * hc + h * 32 + 32, x1);
+        uint32_t v[32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) ss = fmaf(x[t], x[t], ss);
+        for (int t = 0; t < 32; ++t) {
+            ss = fmaf(x0[t], x0[t], ss);
+            v[t] = __float_as_uint(x0[t]);
+        }
+        tmem_st32(lane_base + COL_X + half * hc + h * 32, v);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            ss = fmaf(x1[t], x1[t], ss);
+            v[t] = __float_as_uint(x1[t]);
+        }
+        tmem_st32(lane_base + COL_X + half * hc + h * 32 + 32, v);
     }
+    tmem_wait_st();
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) red[warp] = ss;
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_slot;           // allocated by warp 1 before the barrier above
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
     if (tid == 0) {
         float part = 0.f;
         for (int w = 0; w < NTHREADS / 32; ++w) part += red[w];
@@ -166,47 +183,62 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     bool ok = __syncthreads_and(mbar_wait_cluster(bar_a, 0, WAIT_NS) ? 1 : 0) != 0;
     float tot = 0.f;
     for (int r = 0; r < cs; ++r) tot += norm_part[r];
-    const float nrm = sqrtf(tot) + 1e-7f;
-    for (int h = 0; h < hc / 32; ++h) {
-        const int j0 = half * hc + h * 32;       // within this CTA's columns
-        float xv[32];
-        uint32_t v[32];
-        load32(c0 + j0, xv);
+    const float inv = 1.0f / (sqrtf(tot) + 1e-7f);
+    for (int h = 0; h < hc / 32; h += 2) {
+        uint32_t v[2][32];
+        tmem_ld32(lane_base + COL_X + half * hc + h * 32, v[0]);
+        tmem_ld32(lane_base + COL_X + half * hc + h * 32 + 32, v[1]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-            xv[t] = xv[t] / nrm;
-            v[t] = __float_as_uint(xv[t]);
+        for (int u = 0; u < 2; ++u) {
+            const int j0 = half * hc + (h + u) * 32;       // within this CTA's columns
+            tmem_pin(v[u]);
+            float xv[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                xv[t] = __uint_as_float(v[u][t]) * inv;
+                v[u][t] = __float_as_uint(xv[t]);
+            }
+            tmem_st32(lane_base + COL_X + j0, v[u]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(sm + OFF_X + atom_off(row, c0 + j0 + 8 * c)) = pack8(xv + 8 * c);
         }
-        tmem_st32(lane_base + COL_X + j0, v);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(sm + OFF_X + atom_off(row, c0 + j0 + 8 * c)) = pack8(xv + 8 * c);
     }
     tmem_wait_st();
+    const uint32_t XBLOCK_BYTES = (uint32_t)(cb / 64) * ATOM;
+    // The columns of each half (hc of them, whole atoms) go out to the other
+    // CTAs as soon as that half's 128 threads have written them: a barrier of
+    // the half, then one bulk copy per other CTA from the half's first thread.
+    auto send_half = [&](bool send) {
+        fence_proxy_async_smem();
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory");
+        if (send && (warp & 3) == 0 && lane == 0) {
+            const uint32_t src = base + OFF_X + (uint32_t)((c0 + half * hc) / 64) * ATOM;
+            for (int r = 0; r < cs; ++r)
+                if (r != (int)rank)
+                    bulk_copy_to_cluster(mapa_shared(src, (uint32_t)r), src, XBLOCK_BYTES / 2,
+                                         mapa_shared(barx((int)rank), (uint32_t)r));
+        }
+    };
+    send_half(ok && cs > 1);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t xblock = base + OFF_X + (uint32_t)(c0 / 64) * ATOM;   // this CTA's columns of Xb
-    const uint32_t XBLOCK_BYTES = (uint32_t)(cb / 64) * ATOM;
-    // Own columns of Xb out to the other CTAs; the bytes from CTA r are
-    // counted on barx(r). Send n (n = 0 at set-up, then after iteration n-1)
-    // is consumed by the A GEMM of iteration n, with parity n & 1.
-    int sends = 0;                 // sends made (thread 0's count)
+    // The bytes from CTA r are counted on barx(r): send n (n = 0 at set-up,
+    // then after iteration n-1) is consumed by the A GEMM of iteration n, with
+    // parity n & 1. Thread 0 sets up the count of each incoming send.
+    int sends = 0;                 // sends expected (thread 0's count)
     int waited[MAXCS] = {0, 0, 0, 0};
-    auto send_columns = [&](bool send) {
+    auto expect_columns = [&]() {
         if (tid == 0) {
             for (int r = 0; r < cs; ++r)
                 if (r != (int)rank) mbar_expect_tx(barx(r), XBLOCK_BYTES);
-            if (send)
-                for (int r = 0; r < cs; ++r)
-                    if (r != (int)rank)
-                        bulk_copy_to_cluster(mapa_shared(xblock, (uint32_t)r), xblock, XBLOCK_BYTES,
-                                             mapa_shared(barx((int)rank), (uint32_t)r));
             ++sends;
         }
     };
-    send_columns(ok);
+    expect_columns();
 
     uint32_t phase = 0;
     // Wait for the MMAs just committed; the outcome is made block-uniform so
@@ -268,19 +300,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         arrive_a_done();
         if (ok) {
             // Ab = bf16(A)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t v[32];
-                const int j0 = half * 64 + h * 32;
-                tmem_ld32(lane_base + COL_A + j0, v);
+            {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(lane_base + COL_A + half * 64, v0);
+                tmem_ld32(lane_base + COL_A + half * 64 + 32, v1);
                 tmem_wait_ld();
-                tmem_pin(v);
+                tmem_pin(v0);
+                tmem_pin(v1);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     float x[8];
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) x[t] = __uint_as_float(v[8 * c + t]);
-                    *reinterpret_cast<uint4*>(sm + OFF_A + atom_off(row, j0 + 8 * c)) = pack8(x);
+                    for (int t = 0; t < 8; ++t) x[t] = __uint_as_float(c < 4 ? v0[8 * c + t] : v1[8 * (c - 4) + t]);
+                    *reinterpret_cast<uint4*>(sm + OFF_A + atom_off(row, half * 64 + 8 * c)) = pack8(x);
                 }
             }
             sync_smem();
@@ -297,21 +329,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         }
         if (ok) {
             // Bb = bf16(b A + c AA)
+            uint32_t va[2][32], vaa[2][32];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                uint32_t va[32], vaa[32];
+                tmem_ld32(lane_base + COL_A + half * 64 + h * 32, va[h]);
+                tmem_ld32(lane_base + COL_AA + half * 64 + h * 32, vaa[h]);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
                 const int j0 = half * 64 + h * 32;
-                tmem_ld32(lane_base + COL_A + j0, va);
-                tmem_ld32(lane_base + COL_AA + j0, vaa);
-                tmem_wait_ld();
-                tmem_pin(va);
-                tmem_pin(vaa);
+                tmem_pin(va[h]);
+                tmem_pin(vaa[h]);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float bv[8];
 #pragma unroll
                     for (int t = 0; t < 8; ++t)
-                        bv[t] = fmaf(a.c, __uint_as_float(vaa[8 * c + t]), a.b * __uint_as_float(va[8 * c + t]));
+                        bv[t] = fmaf(a.c, __uint_as_float(vaa[h][8 * c + t]), a.b * __uint_as_float(va[h][8 * c + t]));
                     *reinterpret_cast<uint4*>(sm + OFF_B + atom_off(row, j0 + 8 * c)) = pack8(bv);
                 }
             }
@@ -332,33 +367,44 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         if (!cluster_wait(bar_a, (it + 1) & 1)) ok = false;
         if (ok) {
             // X_j = a X_j + BX_j in TMEM; bf16(X_j) into this CTA's block of Xb
-            for (int h = 0; h < hc / 32; ++h) {
-                const int j0 = half * hc + h * 32;
-                uint32_t vx[32], vb[32];
-                tmem_ld32(lane_base + COL_X + j0, vx);
-                tmem_ld32(lane_base + COL_BX + j0, vb);
-                tmem_wait_ld();
-                tmem_pin(vx);
-                tmem_pin(vb);
-                float xn[32];
+            for (int h = 0; h < hc / 32; h += 2) {
+                // two 32-column pieces per TMEM round trip
+                uint32_t vx[2][32], vb[2][32];
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    xn[t] = fmaf(a.a, __uint_as_float(vx[t]), __uint_as_float(vb[t]));
-                    vx[t] = __float_as_uint(xn[t]);
+                for (int u = 0; u < 2; ++u) {
+                    tmem_ld32(lane_base + COL_X + half * hc + (h + u) * 32, vx[u]);
+                    tmem_ld32(lane_base + COL_BX + half * hc + (h + u) * 32, vb[u]);
                 }
-                tmem_st32(lane_base + COL_X + j0, vx);
+                tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4*>(sm + OFF_X + atom_off(row, c0 + j0 + 8 * c)) = pack8(xn + 8 * c);
+                for (int u = 0; u < 2; ++u) {
+                    tmem_pin(vx[u]);
+                    tmem_pin(vb[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int j0 = half * hc + (h + u) * 32;
+                    float xn[32];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        xn[t] = fmaf(a.a, __uint_as_float(vx[u][t]), __uint_as_float(vb[u][t]));
+                        vx[u][t] = __float_as_uint(xn[t]);
+                    }
+                    tmem_st32(lane_base + COL_X + j0, vx[u]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(sm + OFF_X + atom_off(row, c0 + j0 + 8 * c)) = pack8(xn + 8 * c);
+                }
             }
+            // (after the last iteration each CTA writes back only its own columns)
+            send_half(cs > 1 && it + 1 < a.steps);
             tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // (after the last iteration each CTA writes back only its own columns)
-        if (it + 1 < a.steps) send_columns(ok);
+        if (it + 1 < a.steps) expect_columns();
     }
     if (!ok) {
         if (tid == 0) atomicOr(a.status, ST_TIMEOUT);
