@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--impl", default="lact", choices=["lact", "reference"])
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    # time direct lact_sequence calls instead of a CUDA-graph replay of one
+    p.add_argument("--no-graph", action="store_true")
     # smaller token counts of the same layer (for profiler captures of a small case)
     p.add_argument("--update-tokens", type=int, default=None)
     p.add_argument("--query-tokens", type=int, default=None)
@@ -311,8 +313,8 @@ def main():
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
-    def step():
-        L.lact_sequence(layer.handle, order, q, w.n_q, k, v, e, w.n_kv, w.chunk, o, stream)
+    def step(s=None):
+        L.lact_sequence(layer.handle, order, q, w.n_q, k, v, e, w.n_kv, w.chunk, o, stream if s is None else s)
 
     for _ in range(args.warmup):
         step()
@@ -328,14 +330,14 @@ def main():
     flush = in_bytes < 2 * L2_BYTES
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
 
-    def timed_steps():
+    def timed_steps(run):
         barrier()
         torch.cuda.synchronize(dev)
         if not flush:
             ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ev0.record(stream)
             for _ in range(args.steps):
-                step()
+                run()
             ev1.record(stream)
             torch.cuda.synchronize(dev)
             ms = ev0.elapsed_time(ev1)
@@ -345,20 +347,37 @@ def main():
                 scrub.fill_(1.0)
                 ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 ev0.record(stream)
-                step()
+                run()
                 ev1.record(stream)
                 torch.cuda.synchronize(dev)
                 ms += ev0.elapsed_time(ev1)
         barrier()
         return ms
 
+    # The step as one CUDA graph: lact_sequence captured once (every kernel
+    # and stream fork/join of the call becomes a node) and replayed on the
+    # timing stream, so the timed region holds no host launch overhead. A
+    # replay runs every kernel of the step on the same device buffers, so K
+    # replays are K layer steps (the weights move on each); the results equal
+    # those of direct calls bit for bit.
+    graph, per_step = None, 0
+    if not args.no_graph:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        c0 = L.lact_launch_count()
+        with torch.cuda.graph(graph, stream=cap):
+            step(cap)
+        per_step = L.lact_launch_count() - c0
+        torch.cuda.synchronize(dev)
+
     # region 1: the measured value (no per-phase events in the stream)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.4)
     n0 = L.lact_launch_count()
-    ms_total = max_over_ranks(timed_steps(), pg, dev)
-    launches = L.lact_launch_count() - n0
+    ms_total = max_over_ranks(timed_steps(step if graph is None else graph.replay), pg, dev)
+    launches = L.lact_launch_count() - n0 if graph is None else per_step * args.steps
     ck = clocks.stop()
     ms_step = ms_total / args.steps
     tok = tokens_per_step(w)
@@ -366,7 +385,7 @@ def main():
     # region 2: the same steps with the library's CUDA events around every
     # phase, on the launching stream (per-kernel times for the roofline)
     L.lact_set_profiling(layer.handle, True)
-    ms_prof = max_over_ranks(timed_steps(), pg, dev) / args.steps
+    ms_prof = max_over_ranks(timed_steps(step), pg, dev) / args.steps
     prof = L.lact_get_profile(layer.handle)
     L.lact_set_profiling(layer.handle, False)
 
@@ -431,7 +450,8 @@ def main():
                        "chunk": w.chunk, "order": w.order, "opt": w.opt,
                        "l2": ("L2 flushed before every step (256 MB write, untimed)" if flush
                               else "inputs larger than L2 (no flush)"),
-                       "tflops_per_s": fl["total"] / (ms_step / 1e3) / 1e12 * world},
+                       "tflops_per_s": fl["total"] / (ms_step / 1e3) / 1e12 * world,
+                       "launch": "direct calls" if graph is None else "one CUDA graph replay per step"},
             "roofline": roof,
             "e2e": {"value": job_throughput(tok, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

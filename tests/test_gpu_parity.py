@@ -391,3 +391,47 @@ def test_kernels_write_only_inside_their_buffers(num):
     for buf in [ws_buf, o_buf] + gbufs:
         assert torch.all(buf[:G] == canary) and torch.all(buf[-G:] == canary)
     L.lact_free_state(st)
+
+
+# ------------------------------------------------- CUDA-graph capture of a step
+@pytest.mark.parametrize("num", [1, 2, 5, 8, 10])
+def test_sequence_replayed_from_a_cuda_graph_matches_direct_calls(num):
+    # lact_sequence captured once into a CUDA graph (side-stream fork/join
+    # included) and replayed gives the same outputs and weights, bit for bit,
+    # as a direct call from the same starting weights
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = _small(num)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp)
+    W0 = [None if x is None else to_device(x).unsqueeze(0).repeat(w.B, 1, 1, 1).contiguous()
+          for x in (inp.W1, inp.W2, inp.W3)]
+    q, k, v, e = (to_device(x) for x in (inp.q, inp.k, inp.v, inp.eta))
+    o = torch.empty_like(q)
+    order = L.LACT_CAUSAL_APPLY_THEN_UPDATE if w.order == "causal" else L.LACT_SET_UPDATE_THEN_APPLY
+    s = torch.cuda.Stream()
+
+    def step(stream):
+        L.lact_sequence(layer.handle, order, q, w.n_q, k, v, e, w.n_kv, w.chunk, o, stream)
+
+    def run(fn):
+        with torch.cuda.stream(s):
+            L.lact_set_weights(layer.handle, *W0, s)
+            fn()
+            out = [o.clone()] + [x.clone() for x in layer.weights(s) if x is not None]
+        torch.cuda.synchronize()
+        return out
+
+    direct = run(lambda: step(s))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s)
+    torch.cuda.synchronize()
+    replay = run(lambda: g.replay())
+    assert L.lact_sync_status(layer.handle) == L.LACT_OK
+    for a, b in zip(direct, replay):
+        assert torch.equal(a, b)
+    # and the replay is correct, not merely repeatable
+    errs = compare(w, tuple(None if x is None else to_host_f64(x) for x in replay + [None] * (4 - len(replay))),
+                   O.run_workload(w, inp))
+    assert max(errs.values()) < TOL[w.dtype], errs
