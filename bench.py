@@ -102,8 +102,8 @@ def tokens_per_step(w: li.Workload) -> int:
 # full-size launch of the fused gradient kernel on the million-token layer,
 # from a one-pass ncu capture (summary: profiles/k_grad_tc_million_token_set.md).
 # It describes the kernel source it was taken on, identified by its hash.
-GRAD_TRAFFIC = {"workload": 5, "bytes": 4.45e9 + 134.24e6, "kernel_source": "k_tc_grad.cu",
-                "sha256_prefix": "101eae1112e9d1c5"}
+GRAD_TRAFFIC = {"workload": 5, "bytes": 4454414336 + 134320896, "kernel_source": "k_tc_grad.cu",
+                "sha256_prefix": "83ae3cd43ad83ce0"}
 
 
 def measured_traffic(w: li.Workload, reduced: bool):

@@ -28,6 +28,7 @@ constexpr int LG = 16;          // tokens per tile of the CUDA-core gradient
 template <typename T, typename R>
 __global__ void __launch_bounds__(NT) k_lin_apply_simt(TokView q, T* __restrict__ o, const R* __restrict__ W,
                                                        int d) {
+    pdl_wait();
     extern __shared__ __align__(16) unsigned char smraw[];
     R* qs = reinterpret_cast<R*>(smraw);           // [LT][d]
     const int bh = blockIdx.y;
@@ -56,6 +57,7 @@ __global__ void __launch_bounds__(NT) k_lin_apply_simt(TokView q, T* __restrict_
 template <typename T, typename R, int D>
 __global__ void __launch_bounds__(NT) k_lin_grad_simt(TokView k, TokView v, const float* __restrict__ eta,
                                                       int tps, R* __restrict__ partial, int BH) {
+    pdl_wait();
     __shared__ R ks[LG][D + 1];
     __shared__ R vs[LG][D + 1];
     constexpr int PER = D * D / NT;
@@ -105,6 +107,8 @@ struct LinApplyArgs {
 
 __global__ void __launch_bounds__(128, 1)
 k_lin_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w, const LinApplyArgs a) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[2];
@@ -199,7 +203,7 @@ cudaError_t lin_apply_t(const lact_state* st, TokView q, void* o, cudaStream_t s
     cudaError_t e = cudaFuncSetAttribute(k_lin_apply_simt<T, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((q.n + LT - 1) / LT), st->BH);
-    k_lin_apply_simt<T, R><<<grid, NT, sm, s>>>(q, static_cast<T*>(o), static_cast<const R*>(st->W[0]), d);
+    launch_pdl(k_lin_apply_simt<T, R>, grid, NT, sm, s, q, static_cast<T*>(o), static_cast<const R*>(st->W[0]), d);
     g_launches++;
     return cudaGetLastError();
 }
@@ -216,7 +220,7 @@ cudaError_t lin_grad_t(const lact_state* st, TokView k, TokView v, const float* 
     splits = (ntiles + tps - 1) / tps;
     if (splits < 1) splits = 1;
     dim3 grid((unsigned)splits, st->BH);
-    k_lin_grad_simt<T, R, D><<<grid, NT, 0, s>>>(k, v, eta, tps, static_cast<R*>(st->partial), st->BH);
+    launch_pdl(k_lin_grad_simt<T, R, D>, grid, NT, 0, s, k, v, eta, tps, static_cast<R*>(st->partial), st->BH);
     g_launches++;
     *slots = (int)splits;
     return cudaGetLastError();
@@ -258,7 +262,7 @@ cudaError_t launch_lin_apply(const lact_state* st, TokView q, void* o, cudaStrea
     cudaError_t e = cudaFuncSetAttribute(k_lin_apply_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TSMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((q.n + 127) / 128), BH);
-    k_lin_apply_tc<<<grid, 128, TSMEM, s>>>(mq, mw, la);
+    launch_pdl(k_lin_apply_tc, grid, 128, TSMEM, s, mq, mw, la);
     g_launches++;
     g_tc_launches++;
     return cudaGetLastError();

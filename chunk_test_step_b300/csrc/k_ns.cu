@@ -28,6 +28,7 @@ __device__ __forceinline__ void src_dims(int which, int d, int dh, int& rows, in
 template <typename R>
 __global__ void k_ns_prep(const R* __restrict__ g0, const R* __restrict__ g1,
                           const R* __restrict__ g2, R* __restrict__ X, NsShape sh, R eps) {
+    pdl_wait();
     const int mi = blockIdx.x;
     const int which = mi / sh.BH, bh = mi % sh.BH;
     const R* G = (which == 0 ? g0 : which == 1 ? g1 : g2) + (size_t)bh * sh.d * sh.dh;
@@ -61,6 +62,7 @@ __global__ void k_ns_prep(const R* __restrict__ g0, const R* __restrict__ g1,
 template <typename R>
 __global__ void k_ns_unpack(const R* __restrict__ X, R* __restrict__ g0, R* __restrict__ g1,
                             R* __restrict__ g2, NsShape sh) {
+    pdl_wait();
     const int mi = blockIdx.x;
     const int which = mi / sh.BH, bh = mi % sh.BH;
     R* G = (which == 0 ? g0 : which == 1 ? g1 : g2) + (size_t)bh * sh.d * sh.dh;
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(256) k_bgemm(const R* __restrict__ A, const R*
                                                const R* __restrict__ Cin, R* __restrict__ C,
                                                int M, int N, int K, size_t sA, size_t sB, size_t sC,
                                                int transB, R alpha, R beta) {
+    pdl_wait();
     constexpr int BM = 16 * TPT, BN = 16 * TPT;
     __shared__ R As[BK][BM + 4];
     __shared__ R Bs[BK][BN + 4];
@@ -149,10 +152,10 @@ cudaError_t bgemm(const R* A, const R* B, const R* Cin, R* C, int M, int N, int 
     const int64_t big = (int64_t)((N + 63) / 64) * ((M + 63) / 64) * batch;
     if (big >= 4 * 148) {
         dim3 grid((N + 63) / 64, (M + 63) / 64, batch);
-        k_bgemm<R, 4><<<grid, 256, 0, s>>>(A, B, Cin, C, M, N, K, sA, sB, sC, transB, alpha, beta);
+        launch_pdl(k_bgemm<R, 4>, grid, 256, 0, s, A, B, Cin, C, M, N, K, sA, sB, sC, transB, alpha, beta);
     } else {
         dim3 grid((N + 15) / 16, (M + 15) / 16, batch);
-        k_bgemm<R, 1><<<grid, 256, 0, s>>>(A, B, Cin, C, M, N, K, sA, sB, sC, transB, alpha, beta);
+        launch_pdl(k_bgemm<R, 1>, grid, 256, 0, s, A, B, Cin, C, M, N, K, sA, sB, sC, transB, alpha, beta);
     }
     g_launches++;
     return cudaGetLastError();
@@ -172,7 +175,7 @@ cudaError_t ns_t(const lact_state* st, void* const gv[3], cudaStream_t s) {
     R* Am = static_cast<R*>(st->ns[2]);
     R* Bm = static_cast<R*>(st->ns[3]);
     const size_t sX = (size_t)sh.m * sh.n, sA = (size_t)sh.m * sh.m;
-    k_ns_prep<R><<<batch, 256, 0, s>>>(g[0], g[1], g[2], X, sh, R(1e-7));
+    launch_pdl(k_ns_prep<R>, batch, 256, 0, s, g[0], g[1], g[2], X, sh, R(1e-7));
     g_launches++;
     cudaError_t e = cudaGetLastError();
     for (int it = 0; it < c.ns_steps && e == cudaSuccess; ++it) {
@@ -187,7 +190,7 @@ cudaError_t ns_t(const lact_state* st, void* const gv[3], cudaStream_t s) {
         R* t = X; X = X2; X2 = t;
     }
     if (e != cudaSuccess) return e;
-    k_ns_unpack<R><<<batch, 256, 0, s>>>(X, g[0], g[1], g[2], sh);
+    launch_pdl(k_ns_unpack<R>, batch, 256, 0, s, X, g[0], g[1], g[2], sh);
     g_launches++;
     return cudaGetLastError();
 }

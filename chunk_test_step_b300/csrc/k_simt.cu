@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(NT) k_apply_simt(TokView q, T* __restrict__ o,
                                                    const R* __restrict__ W1,
                                                    const R* __restrict__ W2,
                                                    const R* __restrict__ W3, int dh) {
+    pdl_wait();
     constexpr int TT = Tile<R>::TT, HC = Tile<R>::HC;
     constexpr int DP = D + 1, HP = HC + 1;
     constexpr int G = NT / D;          // token groups in the W2 phase
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(NT) k_grad_simt(TokView k, TokView v, const fl
                                                   const R* __restrict__ W3, int dh,
                                                   int tiles_per_split, R* __restrict__ partial,
                                                   int BH) {
+    pdl_wait();
     constexpr int TT = Tile<R>::TT, HC = Tile<R>::HC;
     constexpr int DP = D + 1, HP = HC + 1;
     constexpr int G = NT / D;          // hidden groups in the accumulation phase
@@ -210,6 +212,7 @@ __global__ void __launch_bounds__(NT) k_grad_simt(TokView k, TokView v, const fl
 template <typename R>
 __global__ void k_reduce(const R* __restrict__ partial, int slots, size_t mat, int nmat, bool accumulate,
                          R* __restrict__ o0, R* __restrict__ o1, R* __restrict__ o2) {
+    pdl_wait();
     const size_t n = (size_t)nmat * mat;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const int m = (int)(i / mat);
@@ -239,7 +242,7 @@ cudaError_t apply_t(const lact_state* st, TokView q, void* o, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((q.n + Tile<R>::TT - 1) / Tile<R>::TT), st->BH);
-    kern<<<grid, NT, sm, s>>>(q, static_cast<T*>(o), static_cast<const R*>(st->W[0]),
+    launch_pdl(kern, grid, NT, sm, s, q, static_cast<T*>(o), static_cast<const R*>(st->W[0]),
                               static_cast<const R*>(st->W[1]), static_cast<const R*>(st->W[2]), st->cfg.dh);
     g_launches++;
     return cudaGetLastError();
@@ -264,7 +267,7 @@ cudaError_t grad_t(const lact_state* st, TokView k, TokView v, const float* eta,
     splits = (ntiles + tps - 1) / tps;
     if (splits < 1) splits = 1;
     dim3 grid((unsigned)splits, dh / HC, st->BH);
-    kern<<<grid, NT, sm, s>>>(k, v, eta, static_cast<const R*>(st->W[0]), static_cast<const R*>(st->W[1]),
+    launch_pdl(kern, grid, NT, sm, s, k, v, eta, static_cast<const R*>(st->W[0]), static_cast<const R*>(st->W[1]),
                               static_cast<const R*>(st->W[2]), dh, tps, static_cast<R*>(st->partial), st->BH);
     g_launches++;
     *slots = (int)splits;
@@ -310,12 +313,12 @@ cudaError_t launch_reduce(const lact_state* st, int slots, bool accumulate, void
     const size_t want = (st->nmat * mat + 255) / 256, cap = (size_t)st->num_sms * 8;
     const int blocks = (int)(want < cap ? want : cap);
     if (st->f64)
-        k_reduce<double><<<blocks, 256, 0, s>>>(static_cast<const double*>(st->partial), slots, mat, st->nmat,
+        launch_pdl(k_reduce<double>, blocks, 256, 0, s, static_cast<const double*>(st->partial), slots, mat, st->nmat,
                                                 accumulate,
                                                 static_cast<double*>(out[0]), static_cast<double*>(out[1]),
                                                 static_cast<double*>(out[2]));
     else
-        k_reduce<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(st->partial), slots, mat, st->nmat, accumulate,
+        launch_pdl(k_reduce<float>, blocks, 256, 0, s, static_cast<const float*>(st->partial), slots, mat, st->nmat, accumulate,
                                                static_cast<float*>(out[0]), static_cast<float*>(out[1]),
                                                static_cast<float*>(out[2]));
     g_launches++;
@@ -349,7 +352,7 @@ cudaError_t grad_raw_d(int dh, int BH, const float* W1, const float* W2, const f
     splits = (ntiles + tps - 1) / tps;
     if (splits < 1) splits = 1;
     dim3 grid((unsigned)splits, dh / HC, BH);
-    kern<<<grid, NT, sm, s>>>(k, v, eta, W1, W2, W3, dh, tps, partial, BH);
+    launch_pdl(kern, grid, NT, sm, s, k, v, eta, W1, W2, W3, dh, tps, partial, BH);
     g_launches++;
     *slots = (int)splits;
     return cudaGetLastError();
@@ -372,7 +375,7 @@ cudaError_t launch_reduce_f32_raw(const float* partial, int slots, size_t mat, f
                                   int num_sms, cudaStream_t s) {
     const size_t want = (3 * mat + 255) / 256, cap = (size_t)num_sms * 8;
     const int blocks = (int)(want < cap ? want : cap);
-    k_reduce<float><<<blocks, 256, 0, s>>>(partial, slots, mat, 3, false, o0, o1, o2);
+    launch_pdl(k_reduce<float>, blocks, 256, 0, s, partial, slots, mat, 3, false, o0, o1, o2);
     g_launches++;
     return cudaGetLastError();
 }

@@ -82,6 +82,8 @@ template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w1,
            const __grid_constant__ CUtensorMap tm_w3, const __grid_constant__ CUtensorMap tm_w2, const ApplyArgs a) {
+    pdl_wait();
+    pdl_trigger();
     typedef ApplyLayout<D> Lo;
     constexpr int NQ = Lo::NQ;
     extern __shared__ __align__(16) unsigned char smraw[];
@@ -329,7 +331,7 @@ static cudaError_t launch_apply_d(const lact_state* st, TokView q, void* o, cuda
     cudaError_t e = cudaFuncSetAttribute(k_apply_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((q.n + TT - 1) / TT), BH);
-    k_apply_tc<D><<<grid, NTHREADS, smem, s>>>(mq, m1, m3, m2, aa);
+    launch_pdl(k_apply_tc<D>, grid, NTHREADS, smem, s, mq, m1, m3, m2, aa);
     g_launches++;
     g_tc_launches++;
     return cudaGetLastError();

@@ -74,6 +74,8 @@ __device__ __forceinline__ float tanh_approx(float x) {
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_apply2_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w1,
             const __grid_constant__ CUtensorMap tm_w3, const __grid_constant__ CUtensorMap tm_w2, const Apply2Args a) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[NBARS];
@@ -330,7 +332,7 @@ cudaError_t launch_apply2_tc(const lact_state* st, TokView q, void* o, cudaStrea
     cudaError_t e = cudaFuncSetAttribute(k_apply2_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((q.n + NSUB * 128 - 1) / (NSUB * 128)), BH);
-    k_apply2_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, m1, m3, m2, aa);
+    launch_pdl(k_apply2_tc, grid, NTHREADS, SMEM_BYTES, s, mq, m1, m3, m2, aa);
     g_launches++;
     g_tc_launches++;
     return cudaGetLastError();

@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 k_fwdbwd_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w3,
             const __grid_constant__ CUtensorMap tm_w2, const FbArgs a) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[NBARS];
@@ -377,7 +379,7 @@ cudaError_t launch_fwdbwd_tc(const lact_state* st, TokView k, TokView v, const f
     cudaError_t e = cudaFuncSetAttribute(k_fwdbwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(dh / HB), (unsigned)splits, (unsigned)BH);
-    k_fwdbwd_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(mk, mv, m1, m3, m2, fa);
+    launch_pdl(k_fwdbwd_tc, grid, NTHREADS, SMEM_BYTES, s, mk, mv, m1, m3, m2, fa);
     g_launches++;
     g_tc_launches++;
     return cudaGetLastError();

@@ -80,6 +80,8 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t mbar, sync_a, sync_x[MAXCS];
@@ -477,13 +479,15 @@ cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s)
     lc.blockDim = dim3(NTHREADS);
     lc.dynamicSmemBytes = SMEM_BYTES;
     lc.stream = s;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = (unsigned)cs;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait()
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = at;
-    lc.numAttrs = 1;
+    lc.numAttrs = 2;
     e = cudaLaunchKernelEx(&lc, k_ns_tc, a);
     g_launches++;
     g_tc_launches++;

@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
            const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1,
            const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap tb2, const WArgs a) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[NBARS];
@@ -296,7 +298,7 @@ cudaError_t launch_wgrad_tc(const lact_state* st, TokView k, TokView v, const bf
     cudaError_t e = cudaFuncSetAttribute(k_wgrad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)total, (unsigned)BH, 1);
-    k_wgrad_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(ma[0], mb[0], ma[1], mb[1], ma[2], mb[2], wa);
+    launch_pdl(k_wgrad_tc, grid, NTHREADS, SMEM_BYTES, s, ma[0], mb[0], ma[1], mb[1], ma[2], mb[2], wa);
     g_launches++;
     g_tc_launches++;
     return cudaGetLastError();
@@ -349,7 +351,7 @@ cudaError_t launch_lin_grad_tc(const lact_state* st, TokView k, TokView v, const
     cudaError_t e = cudaFuncSetAttribute(k_wgrad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)wa.tiles[0], (unsigned)BH, (unsigned)splits);
-    k_wgrad_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(mv, mk, mv, mk, mv, mk, wa);
+    launch_pdl(k_wgrad_tc, grid, NTHREADS, SMEM_BYTES, s, mv, mk, mv, mk, mv, mk, wa);
     g_launches++;
     g_tc_launches++;
     *slots = (int)splits;

@@ -60,6 +60,7 @@ __device__ __forceinline__ void store_vec(double* p, const double* v, int n) {
 
 template <typename R, int VEC>
 __global__ void __launch_bounds__(256) k_update_renorm(UpdArgs<R> a) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t r0 = (int64_t)a.BH * a.rows[0], r1 = (int64_t)a.BH * a.rows[1];
@@ -134,12 +135,14 @@ __global__ void __launch_bounds__(256) k_update_renorm(UpdArgs<R> a) {
 }
 
 __global__ void k_shadow(const float* __restrict__ W, bf16* __restrict__ S, size_t n) {
+    pdl_wait();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
         S[i] = __float2bfloat16_rn(W[i]);
 }
 
 template <typename A, typename B>
 __global__ void k_convert(const A* __restrict__ src, B* __restrict__ dst, size_t n) {
+    pdl_wait();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
         dst[i] = (B)src[i];
 }
@@ -164,8 +167,8 @@ cudaError_t update_t(const lact_state* st, const void* const g[3], double scale,
     const int64_t rows = (int64_t)st->BH * (a.rows[0] + a.rows[1] + a.rows[2]);
     const int blocks = (int)((rows * 32 + 255) / 256);
     // every row length here is a multiple of 32; float4 when a multiple of 128
-    if (sizeof(R) == 4 && d % 128 == 0 && dh % 128 == 0) k_update_renorm<R, 4><<<blocks, 256, 0, s>>>(a);
-    else k_update_renorm<R, 1><<<blocks, 256, 0, s>>>(a);
+    if (sizeof(R) == 4 && d % 128 == 0 && dh % 128 == 0) launch_pdl(k_update_renorm<R, 4>, blocks, 256, 0, s, a);
+    else launch_pdl(k_update_renorm<R, 1>, blocks, 256, 0, s, a);
     g_launches++;
     return cudaGetLastError();
 }
@@ -181,7 +184,7 @@ cudaError_t launch_shadow(const lact_state* st, cudaStream_t s) {
     if (st->cfg.io_dtype != LACT_BF16) return cudaSuccess;
     const size_t n = (size_t)st->BH * st->cfg.d * st->cfg.dh;
     for (int m = 0; m < st->nmat; ++m) {
-        k_shadow<<<st->num_sms * 4, 256, 0, s>>>(static_cast<const float*>(st->W[m]), st->Wsh[m], n);
+        launch_pdl(k_shadow, st->num_sms * 4, 256, 0, s, static_cast<const float*>(st->W[m]), st->Wsh[m], n);
         g_launches++;
     }
     return cudaGetLastError();
@@ -191,13 +194,13 @@ cudaError_t launch_convert(const void* src, bool src_f64, void* dst, bool dst_f6
                            cudaStream_t s) {
     const int blocks = num_sms * 4;
     if (src_f64 && dst_f64)
-        k_convert<double, double><<<blocks, 256, 0, s>>>(static_cast<const double*>(src), static_cast<double*>(dst), n);
+        launch_pdl(k_convert<double, double>, blocks, 256, 0, s, static_cast<const double*>(src), static_cast<double*>(dst), n);
     else if (src_f64)
-        k_convert<double, float><<<blocks, 256, 0, s>>>(static_cast<const double*>(src), static_cast<float*>(dst), n);
+        launch_pdl(k_convert<double, float>, blocks, 256, 0, s, static_cast<const double*>(src), static_cast<float*>(dst), n);
     else if (dst_f64)
-        k_convert<float, double><<<blocks, 256, 0, s>>>(static_cast<const float*>(src), static_cast<double*>(dst), n);
+        launch_pdl(k_convert<float, double>, blocks, 256, 0, s, static_cast<const float*>(src), static_cast<double*>(dst), n);
     else
-        k_convert<float, float><<<blocks, 256, 0, s>>>(static_cast<const float*>(src), static_cast<float*>(dst), n);
+        launch_pdl(k_convert<float, float>, blocks, 256, 0, s, static_cast<const float*>(src), static_cast<float*>(dst), n);
     g_launches++;
     return cudaGetLastError();
 }

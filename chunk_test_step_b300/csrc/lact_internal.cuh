@@ -77,6 +77,37 @@ namespace lact {
 extern std::atomic<int64_t> g_launches;      // every kernel launch of this library
 extern std::atomic<int64_t> g_tc_launches;   // launches of tcgen05 tensor-core kernels
 
+// ------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream
+// serialization, so the GPU may start launching it before the kernel ahead
+// of it in the stream has finished. Each kernel calls pdl_wait() before it
+// touches global memory: griddepcontrol.wait blocks until the previous kernel
+// has completed and its writes are visible, so no kernel reads data early;
+// what overlaps is the launch and the CTAs' arrival on the SMs.
+// The tensor-core kernels also call pdl_trigger() at once, which lets the
+// next kernel launch as soon as every CTA of theirs is running: its CTAs then
+// wait in place of an SM that would otherwise idle in the last wave. The
+// CUDA-core kernels leave the trigger to their exit, so that waiting CTAs
+// never share an SM with their arithmetic.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kern, static_cast<Args&&>(args)...);
+}
+
 // ---------------------------------------------------------------- helpers
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }

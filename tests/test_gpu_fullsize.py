@@ -1,5 +1,7 @@
 """Full-size parity: every workload at its own size, in the launch
-configuration bench.py times (one lact_sequence call, max_chunk = chunk).
+configuration bench.py times (one lact_sequence call, max_chunk = chunk; for
+the bf16 workloads the call captured as a CUDA graph and replayed, as the
+bench times it).
 
 The tiny fp32 workloads are compared with the oracle element by element.
 For the bf16 workloads the oracle cannot run inside a test (the
@@ -44,7 +46,14 @@ def test_bf16_workloads_full_size_sampled(num):
     layer = L.LactLayer(config_for(w), to_device(inp.W1), to_device(inp.W2), to_device(inp.W3))
     q, k, v, e = (to_device(x) for x in (inp.q, inp.k, inp.v, inp.eta))
     order = L.LACT_CAUSAL_APPLY_THEN_UPDATE if w.order == "causal" else L.LACT_SET_UPDATE_THEN_APPLY
-    o = layer.sequence(order, q, k, v, e, w.chunk)
+    o = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        L.lact_sequence(layer.handle, order, q, w.n_q, k, v, e, w.n_kv, w.chunk, o, s)
+    torch.cuda.synchronize()
+    g.replay()              # the one step, from the initial weights
     W = layer.weights()
     torch.cuda.synchronize()
     assert L.lact_sync_status(layer.handle) == L.LACT_OK
