@@ -360,16 +360,21 @@ def main():
     # replay runs every kernel of the step on the same device buffers, so K
     # replays are K layer steps (the weights move on each); the results equal
     # those of direct calls bit for bit.
-    graph, per_step = None, 0
+    graph, per_step, launch_mode = None, 0, "direct calls"
     if not args.no_graph:
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        c0 = L.lact_launch_count()
-        with torch.cuda.graph(graph, stream=cap):
-            step(cap)
-        per_step = L.lact_launch_count() - c0
-        torch.cuda.synchronize(dev)
+        try:
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            c0 = L.lact_launch_count()
+            with torch.cuda.graph(g, stream=cap):
+                step(cap)
+            per_step = L.lact_launch_count() - c0
+            torch.cuda.synchronize(dev)
+            graph, launch_mode = g, "one CUDA graph replay per step"
+        except RuntimeError as exc:   # capture refused: time direct calls instead, and say so
+            torch.cuda.synchronize(dev)
+            launch_mode = f"direct calls (graph capture failed: {str(exc).splitlines()[0][:120]})"
 
     # region 1: the measured value (no per-phase events in the stream)
     clocks = ClockSampler(local)
@@ -451,7 +456,7 @@ def main():
                        "l2": ("L2 flushed before every step (256 MB write, untimed)" if flush
                               else "inputs larger than L2 (no flush)"),
                        "tflops_per_s": fl["total"] / (ms_step / 1e3) / 1e12 * world,
-                       "launch": "direct calls" if graph is None else "one CUDA graph replay per step"},
+                       "launch": launch_mode},
             "roofline": roof,
             "e2e": {"value": job_throughput(tok, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
