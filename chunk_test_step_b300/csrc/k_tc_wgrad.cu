@@ -195,10 +195,15 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
                 ne_next = eta_row(i + 1);
                 if (*abort_v || !mbar_wait_warp(bar(B_F + s), (i / STAGES) & 1, WAIT_NS)) { give_up(); break; }
                 uint4* rp = reinterpret_cast<uint4*>(sm + s * STAGE_BYTES + blk * BOXB + trow * 128);
+                // the 8 chunks of the row in an order rotated by lane, so that
+                // the 32 rows of a warp (128 bytes apart) spread over all
+                // banks; all loads first, then all stores
+                uint4 x[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 x = rp[c];
-                    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+                for (int c0 = 0; c0 < 8; ++c0) x[c0] = rp[(c0 + lane) & 7];
+#pragma unroll
+                for (int c0 = 0; c0 < 8; ++c0) {
+                    uint32_t* w = reinterpret_cast<uint32_t*>(&x[c0]);
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&w[u]);
@@ -206,8 +211,9 @@ k_wgrad_tc(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUte
                         pr = __floats2bfloat162_rn(f.x * ne, f.y * ne);
                         w[u] = *reinterpret_cast<uint32_t*>(&pr);
                     }
-                    rp[c] = x;
                 }
+#pragma unroll
+                for (int c0 = 0; c0 < 8; ++c0) rp[(c0 + lane) & 7] = x[c0];
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_S + s));
