@@ -178,11 +178,18 @@ k_lin_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
                 pk[j / 2] = *reinterpret_cast<uint32_t*>(&p);
             }
-            if (tok < a.n) {
-                uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)bh * a.n_total + a.t0 + tok) * TD + h * 32);
+            // four lanes store one row's 64 bytes together after a transpose
+            // within each quad of lanes (whole 32-byte sectors per warp store)
+            uint4 ch[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            }
+            for (int c = 0; c < 4; ++c) ch[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            quad_transpose(ch, lane);
+            const int64_t quad_tok = tok - (lane & 3);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+                if (quad_tok + k4 < a.n)
+                    *reinterpret_cast<uint4*>(a.o + ((int64_t)bh * a.n_total + a.t0 + quad_tok + k4) * TD + h * 32 +
+                                              8 * (lane & 3)) = ch[k4];
         }
     } else if (tid == 0 && !done) {
         atomicOr(a.status, ST_TIMEOUT);

@@ -273,13 +273,20 @@ k_apply_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 tmem_pin(v);
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) packed[j / 2] = pack_bf16(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-                if (tok < a.n) {
-                    uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)bh * a.n_total + a.t0 + tok) * D + hf * (D / 2) +
-                                                          h * 32);
+                // 64 contiguous bytes of this thread's row; after a transpose
+                // within each quad of lanes, four lanes store one row's 64 bytes
+                // together (whole 32-byte sectors per warp store)
+                uint4 ch[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-                }
+                for (int c = 0; c < 4; ++c)
+                    ch[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                quad_transpose(ch, lane);
+                const int64_t quad_tok = tok - (lane & 3);
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    if (quad_tok + k4 < a.n)
+                        *reinterpret_cast<uint4*>(a.o + ((int64_t)bh * a.n_total + a.t0 + quad_tok + k4) * D + hf * (D / 2) +
+                                                  h * 32 + 8 * (lane & 3)) = ch[k4];
             }
         } else if (ok) {
             give_up();

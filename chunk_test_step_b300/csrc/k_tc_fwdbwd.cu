@@ -101,27 +101,6 @@ __device__ __forceinline__ uint32_t pack_f2(f2 v) {
     return pack_bf16(lo, hi);
 }
 
-__device__ __forceinline__ uint4 shfl_xor_u4(uint4 v, int mask) {
-    return make_uint4(__shfl_xor_sync(0xffffffffu, v.x, mask), __shfl_xor_sync(0xffffffffu, v.y, mask),
-                      __shfl_xor_sync(0xffffffffu, v.z, mask), __shfl_xor_sync(0xffffffffu, v.w, mask));
-}
-
-// 4 x 4 transpose of 16-byte chunks within each quad of lanes. On entry lane
-// 4m + g holds chunks 0..3 of its own row; on exit it holds chunk g of rows
-// 4m .. 4m + 3 (c[k] = row 4m + k). Two exchanges: chunk pairs with the lane
-// two apart, then single chunks with the neighbouring lane.
-__device__ __forceinline__ void quad_transpose(uint4 (&c)[4], int lane) {
-    const bool b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
-    {
-        const uint4 r0 = shfl_xor_u4(b1 ? c[0] : c[2], 2), r1 = shfl_xor_u4(b1 ? c[1] : c[3], 2);
-        if (b1) { c[0] = r0; c[1] = r1; } else { c[2] = r0; c[3] = r1; }
-    }
-    {
-        const uint4 r0 = shfl_xor_u4(b0 ? c[0] : c[1], 1), r1 = shfl_xor_u4(b0 ? c[2] : c[3], 1);
-        if (b0) { c[0] = r0; c[2] = r1; } else { c[1] = r0; c[3] = r1; }
-    }
-}
-
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_fwdbwd_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w3,
