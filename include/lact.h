@@ -31,6 +31,14 @@
  *    word that lact_sync_status() reads.
  *  - No exception or process exit crosses this interface.
  *  - A state must not be used from two host threads at once.
+ *  - The compute calls (lact_chunk_apply, lact_chunk_update, lact_sequence,
+ *    lact_chunk_gradient, lact_apply_gradient, lact_set_weights) enqueue only
+ *    kernels, copies, event records and stream waits, so with profiling off
+ *    they may be recorded by stream capture into a CUDA graph; a replay repeats the recorded work on
+ *    the same buffers (the state's weights move on with each replay) and gives
+ *    the same results as the direct call. Kernels are launched with
+ *    programmatic stream serialization and wait for the kernel ahead of them
+ *    before touching memory.
  */
 #ifndef LACT_H
 #define LACT_H
