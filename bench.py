@@ -242,10 +242,14 @@ def cpu_baseline(w: li.Workload, seconds: float = 15.0, sample: li.Workload | No
     s1 = sample or size_sample(w, seconds)
     dt = time_oracle(s1)
     toks = tokens_per_step(s1)
-    return {"value": toks / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+    # A layer token is worked on by every one of the layer's H heads, and the
+    # oracle takes one (b, h) after another: the layer's rate is the sample's
+    # per-head rate over H (batch entries scale tokens and time alike).
+    return {"value": toks / dt / w.H, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
             "sample": f"1 (b,h) of the workload: {s1.n_kv} update + {s1.n_q if s1.order == 'set' else 0} "
                       f"query tokens, d={s1.d}, dh={s1.dh}, {s1.opt}, {s1.order}; fp64 numpy/OpenBLAS; "
-                      f"{dt:.2f} s; value = sample tokens / time",
+                      f"{dt:.2f} s; value = sample tokens / (time x {w.H} heads), the oracle taking one "
+                      f"(b, h) at a time",
             "seconds": dt}
 
 
