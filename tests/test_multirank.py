@@ -65,3 +65,24 @@ def test_reference_arm_prints_on_rank_zero_only(monkeypatch, capsys):
         steps, warmup, gpus = 1, 0, 2
     assert bench.run_reference(Args(), li.WORKLOADS[1]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_has_the_contract_keys():
+    # rank 0 of a one-process run prints one JSON line in the bench's unit
+    import json
+    import subprocess
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "1",
+                          "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=600,
+                         env={k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")})
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
+    assert d["config"]["workload"] == "tiny-causal-f32-gd"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and "sample" in cb
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
