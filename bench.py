@@ -371,7 +371,9 @@ def main():
             cap.wait_stream(stream)
             g = torch.cuda.CUDAGraph()
             c0 = L.lact_launch_count()
-            with torch.cuda.graph(g, stream=cap):
+            # thread-local capture: CUDA calls of other host threads (a
+            # communicator's watchdog) do not invalidate it
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
                 step(cap)
             per_step = L.lact_launch_count() - c0
             torch.cuda.synchronize(dev)
