@@ -8,8 +8,9 @@
 //
 // (LaCT review page, "Local attention and nonlinear memory work together":
 // the updated fast weights are L2-normalised; each row keeps the norm it had
-// before the update.) A row whose new norm is 0 is left as it is; a
-// non-finite norm sets the sticky status bit ST_NONFINITE.
+// before the update.) A row whose updated norm is 0 cannot be rescaled: it
+// is stored as updated (the zero row, factor 1); a non-finite norm sets the
+// sticky status bit ST_NONFINITE.
 //
 // One warp per row; rows are contiguous in memory (W1, W3: dh rows of d;
 // W2: d rows of dh). HBM-bound: reads W and D, writes W' and its bf16 copy.

@@ -364,3 +364,93 @@ def test_linear_causal_and_set_orders():
     W_exp = O.renorm_update(W[0], -O.linear_chunk_gradient(W[0], K, V, eta))
     np.testing.assert_allclose(W2[0], W_exp, rtol=1e-14)
     np.testing.assert_allclose(o2, Q @ W_exp.T, rtol=1e-13)
+
+
+# ------------------------------------------------------------- Muon step
+def test_muon_step_lowers_the_chunk_loss_for_a_small_rate():
+    # A Muon step moves every matrix against its gradient: <dL/dW, NS5(dL/dW)>
+    # is the sum of the gradient's singular values times positive quintic
+    # images of them, so for a small rate the chunk loss (pinned above by
+    # finite differences) drops, and by the first-order amount <g, D>.
+    W1, W2, W3, K, V, eta = _tiny(n=16, seed=21)
+    W = (W1, W2, W3)
+    L0 = O.chunk_loss(*W, K, V, eta)
+    g = O.chunk_gradient(*W, K, V, eta)
+    for lr in (1e-4, 1e-3):
+        D = [O.optimizer_delta(gm, "muon", lr=lr) for gm in g]
+        first_order = sum(float(np.sum(gm * Dm)) for gm, Dm in zip(g, D))
+        assert first_order < 0.0
+        L1 = O.chunk_loss(*(Wm + Dm for Wm, Dm in zip(W, D)), K, V, eta)
+        assert L1 < L0
+        assert abs((L1 - L0) - first_order) < 0.05 * abs(first_order)
+
+
+@pytest.mark.parametrize("shape", [(6, 10), (10, 6)])
+def test_muon_step_is_minus_lr_times_the_quintic_spectrum(shape):
+    # For G = U diag(s) V^T the step is -lr U diag(phi(s / |s|)) V^T, phi the
+    # scalar quintic map applied five times: the rate scales it, the sign is
+    # negative, and the singular vectors are the gradient's. The bf16 rounding
+    # points move the spectrum by a few percent on small matrices (the
+    # closed-form test above allows 8e-2 for the same reason).
+    g = np.random.default_rng(22)
+    m, n = shape
+    k = min(m, n)
+    U, V = _orth(m, g), _orth(n, g)
+    s = np.sort(g.uniform(0.5, 2.0, size=k))[::-1]
+    G = U[:, :k] @ np.diag(s) @ V[:, :k].T
+    phi = _scalar_ns(s / (np.linalg.norm(s) + O.NS_EPS))
+    for lr in (0.02, 0.5):
+        D = O.optimizer_delta(G, "muon", lr=lr)
+        core = U[:, :k].T @ D @ V[:, :k]            # diag(-lr phi) up to rounding drift
+        want = -lr * np.diag(phi)
+        assert np.linalg.norm(core - want) / np.linalg.norm(want) < 8e-2
+        # next to nothing outside the gradient's singular subspaces (only the
+        # rounding of the bf16 operands leaks there)
+        inside = U[:, :k] @ core @ V[:, :k].T
+        assert np.linalg.norm(D - inside) / np.linalg.norm(D) < 2e-2
+
+
+def test_gd_step_is_minus_the_gradient():
+    g = np.random.default_rng(23).normal(size=(5, 7))
+    np.testing.assert_array_equal(O.optimizer_delta(g, "gd"), -g)
+
+
+def test_renorm_of_a_row_updated_to_zero_stores_the_zero_row():
+    # a row whose updated norm is 0 cannot be rescaled to its old norm: it is
+    # stored as updated (zero), not restored
+    W = np.array([[3.0, 4.0], [1.0, -2.0]])
+    D = np.array([[-3.0, -4.0], [0.5, 0.5]])
+    out = O.renorm_update(W, D)
+    assert np.all(out[0] == 0.0)
+    np.testing.assert_allclose(np.linalg.norm(out[1]), np.linalg.norm(W[1]), rtol=1e-15)
+
+
+# ------------------------------------------------------- whole-workload driver
+def test_run_workload_gives_every_batch_entry_its_heads_initial_weights():
+    # Two batch entries x two heads, built by hand: entry 1 repeats entry 0's
+    # tokens, the heads have different initial weights. The fast weights are
+    # per (b, h), initialised from head h for every b: both entries of a head
+    # end identical, the heads differ, and the first causal chunk of (b, h)
+    # reads head h's initial weights (brute-force readout loops above pin
+    # fast_weight_apply).
+    import lact_inputs as li
+    g = np.random.default_rng(24)
+    d, dh, n, ch = 4, 8, 6, 3
+    w = li.Workload(0, "hand-built", 2, 2, d, dh, "f32", "causal", "gd", n, n, ch, 0)
+    tok = lambda: np.repeat(g.normal(size=(1, 2, n, d)).astype(np.float32), 2, axis=0)
+    q, k, v = tok(), tok(), tok()
+    eta = np.repeat((0.05 + 0.01 * g.random((1, 2, n))).astype(np.float32), 2, axis=0)
+    Wh = [(g.normal(size=s) * 0.5).astype(np.float32) for s in ((2, dh, d), (2, d, dh), (2, dh, d))]
+    inp = li.Inputs(q, k, v, eta, *Wh)
+    O_, W1, W2, W3 = O.run_workload(w, inp)
+    for Wf in (O_, W1, W2, W3):
+        np.testing.assert_array_equal(Wf[0], Wf[1])
+        assert not np.allclose(Wf[0, 0], Wf[0, 1])
+    for b in range(2):
+        for h in range(2):
+            first = O.fast_weight_apply(*(x[h].astype(np.float64) for x in Wh), q[b, h, :ch].astype(np.float64))
+            np.testing.assert_allclose(O_[b, h, :ch], first, rtol=1e-13)
+    # only the listed heads are computed
+    O2, *_ = O.run_workload(w, inp, heads=[(1, 0)])
+    np.testing.assert_array_equal(O2[1, 0], O_[1, 0])
+    assert np.all(O2[0] == 0.0) and np.all(O2[1, 1] == 0.0)
