@@ -21,7 +21,7 @@ import pytest
 
 import lact_inputs as li
 from oracle import lact_oracle as O
-from tests.harness import TOL, compare, config_for, rel_l2, run_gpu, to_device
+from tests.harness import TOL, compare, compare_change, config_for, dw_tol, initial_weights, record, rel_l2, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
@@ -31,8 +31,11 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 def test_tiny_workloads_full_size(num):
     w = li.WORKLOADS[num]
     inp = li.make_inputs(w)
-    errs = compare(w, run_gpu(w, inp), O.run_workload(w, inp))
+    got, want = run_gpu(w, inp), O.run_workload(w, inp)
+    errs = compare(w, got, want, "fullsize")
     assert max(errs.values()) < TOL[w.dtype], errs
+    dW = compare_change(w, initial_weights(w, inp), got[1:], want[1:], exact_gradient=False, test="fullsize")
+    assert max(dW.values()) < dw_tol(w, False), dW
 
 
 @pytest.mark.parametrize("num", [2, 4, 5, 7, 8, 10])
@@ -58,17 +61,31 @@ def test_bf16_workloads_full_size_sampled(num):
     torch.cuda.synchronize()
     assert L.lact_sync_status(layer.handle) == L.LACT_OK
     W0 = (inp.W1, inp.W2, inp.W3)
+    worst = {}
+    tol_dw = dw_tol(w, exact_gradient=False)
     for head in doc["heads"]:
         b, h, rows = head["b"], head["h"], head["rows"]
         got_o = o[b, h, rows["o"]].double().cpu().numpy()
         err = rel_l2(got_o, np.array(head["o"]))
+        worst["o"] = max(worst.get("o", 0.0), err)
         assert err < TOL["bf16"], ("o", b, h, err)
         for m, name in enumerate(("W1", "W2", "W3")):
             if W[m] is None:
                 continue
             got = W[m][b, h, rows[name]].double().cpu().numpy()
-            err = rel_l2(got, np.array(head[name]))
+            want = np.array(head[name])
+            err = rel_l2(got, want)
+            worst[name] = max(worst.get(name, 0.0), err)
             assert err < TOL["bf16"], (name, b, h, err)
+            # the change of the sampled rows over the call (initial rows are
+            # the generator's, the final ones the oracle's)
+            w0 = W0[m][h, rows[name]].astype(np.float64)
+            chg = rel_l2(got - w0, want - w0)
+            worst["d" + name] = max(worst.get("d" + name, 0.0), chg)
+            assert chg < tol_dw, ("d" + name, b, h, chg)
+    for name, err in worst.items():
+        record("fullsize_sampled", w, name, err, tol_dw if name.startswith("d") else TOL["bf16"],
+               **({"kind": "change"} if name.startswith("d") else {}))
     # every row keeps its initial norm
     for m in range(3):
         if W[m] is None:
