@@ -30,24 +30,27 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices] = {};   // device address of g_scratch, per device
-int g_num_sms[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};   // SM count per device (a property of the device, kept)
 
-// Device address of g_scratch on the current device, looked up once per
-// device (host code may not use g_scratch's name as a device pointer).
+// Device address of g_scratch on the current device (host code may not use
+// g_scratch's name as a device pointer). Looked up on every call, so that a
+// context torn down and recreated (cudaDeviceReset) never leaves a stale
+// address behind; once this file's module is loaded on the device the lookup
+// allocates nothing. The module itself (with the array) is loaded by the
+// first lookup on each device when CUDA loads modules lazily, which is an
+// allocation: hence the warm-up call the header asks for.
 lact_status scratch_for_current_device(float** out, int* num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LACT_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return LACT_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return LACT_ERR_CUDA;
+    if (!g_num_sms[dev]) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LACT_ERR_CUDA;
-        g_scratch_addr[dev] = p;
         g_num_sms[dev] = sms;
     }
-    *out = static_cast<float*>(g_scratch_addr[dev]);
+    *out = static_cast<float*>(p);
     *num_sms = g_num_sms[dev];
     return LACT_OK;
 }
@@ -67,6 +70,7 @@ extern "C" lact_status lact_chunk_gradient_noalloc(const lact_config* cfg, const
     if (!(cfg->d == 32 || cfg->d == 64 || cfg->d == 128 || cfg->d == 256)) return LACT_ERR_INVALID_ARG;
     if (cfg->dh < 64 || cfg->dh > 1024 || cfg->dh % 64 != 0) return LACT_ERR_INVALID_ARG;
     if (cfg->io_dtype != LACT_BF16) return LACT_ERR_UNSUPPORTED;
+    if (cfg->memory != LACT_MEM_SWIGLU) return LACT_ERR_UNSUPPORTED;   // SwiGLU memory only
     if (n_tok < 0) return LACT_ERR_INVALID_ARG;
     const void* ptrs[] = {d_W1, d_W2, d_W3, d_dW1, d_dW2, d_dW3};
     for (const void* p : ptrs)

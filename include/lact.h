@@ -125,17 +125,28 @@ lact_status lact_init_state(lact_state** out, const lact_config* cfg, void* d_wo
                             const float* d_W3, cudaStream_t stream);
 
 /* Readout (apply): o_i = f_W(q_i) with the current W, for n_q query tokens
- * per (b, h). d_q, d_o: [B, H, n_q, d] io dtype. n_q = 0 enqueues nothing. */
+ * per (b, h). d_q, d_o: [B, H, n_q, d] io dtype. n_q = 0 enqueues nothing.
+ * (Review page, "Fast weights are temporary context memory": a query reads
+ * the key-value relation stored in the small network's weights; "Local
+ * attention and nonlinear memory work together": that network is the
+ * three-matrix SwiGLU MLP.) */
 lact_status lact_chunk_apply(lact_state* st, const void* d_q, int64_t n_q, void* d_o,
                              cudaStream_t stream);
 
 /* One update of W on one chunk of n_tok tokens per (b, h) (0 <= n_tok <=
  * max_chunk): chunk gradient, optimiser step, row renorm. d_k, d_v:
- * [B, H, n_tok, d] io dtype; d_eta: [B, H, n_tok] fp32. */
+ * [B, H, n_tok, d] io dtype; d_eta: [B, H, n_tok] fp32.
+ * (Review page, "Local attention and nonlinear memory work together": the
+ * negative inner-product loss over the chunk with token-specific learning
+ * rates, the GD / momentum / Muon update and the L2-normalised result;
+ * "Test-Time Training Done Right", abstract: one update per chunk of 2K to
+ * ~1M tokens.) */
 lact_status lact_chunk_update(lact_state* st, const void* d_k, const void* d_v,
                               const float* d_eta, int64_t n_tok, cudaStream_t stream);
 
-/* A whole layer call.
+/* A whole layer call (review page, "Update order must respect the task":
+ * language chunks read the memory of earlier chunks and then update it;
+ * a posed image set is absorbed whole before its queries are answered).
  * LACT_CAUSAL_APPLY_THEN_UPDATE: q and k/v are the same n = n_q = n_kv
  *   tokens, cut into chunks of `chunk` (the last may be shorter); each chunk
  *   is first read with the current W (into d_o), then W is updated on it.
@@ -186,7 +197,8 @@ lact_status lact_import_state(lact_state* st, const void* d_src, size_t bytes, c
  * path that must not fail for lack of memory or synchronise the device), so
  * cannot provide the workspace lact_init_state asks for.
  *
- * Computes what lact_chunk_gradient computes, for bf16 io only:
+ * Computes what lact_chunk_gradient computes, for bf16 io and the SwiGLU
+ * memory only (anything else returns LACT_ERR_UNSUPPORTED):
  * d_dW1 [B,H,dh,d], d_dW2 [B,H,d,dh], d_dW3 [B,H,dh,d] (fp32 outputs) from
  * the fp32 weights d_W1 [B,H,dh,d], d_W2 [B,H,d,dh], d_W3 [B,H,dh,d] and
  * d_k, d_v [B,H,n_tok,d] bf16, d_eta [B,H,n_tok] fp32 (inputs), on the
@@ -194,11 +206,16 @@ lact_status lact_import_state(lact_state* st, const void* d_src, size_t bytes, c
  * device memory inside this library, held by every GPU that loads it until
  * the process exits; one split slot takes 12*B*H*d*dh bytes, and a problem
  * whose slot does not fit returns LACT_ERR_UNSUPPORTED before anything runs.
- * The first call on each device looks up that array's device address (make
- * it before any stream capture). All calls share the array: two calls that
- * may overlap on the GPU (other streams, other host threads) race, so order
- * them on one stream. Nothing in it needs clearing: each call overwrites what
- * it reads. Calls no cudaMalloc, cudaFree or other allocating routine. */
+ * Each call looks up that array's device address. CUDA loads a library's
+ * device code lazily by default, and the first call on each device is what
+ * loads the part holding the array: that load allocates device memory (the
+ * array, the code) and may synchronise. So make one warm-up call per device
+ * outside any path that must not allocate, and before any stream capture (or
+ * run the process with CUDA_MODULE_LOADING=EAGER); later calls allocate
+ * nothing. All calls share the array: two calls that may overlap on the GPU
+ * (other streams, other host threads) race, so order them on one stream.
+ * Nothing in it needs clearing: each call overwrites what it reads. Calls no
+ * cudaMalloc, cudaFree or other allocating routine. */
 lact_status lact_chunk_gradient_noalloc(const lact_config* cfg, const float* d_W1, const float* d_W2,
                                         const float* d_W3, const void* d_k, const void* d_v,
                                         const float* d_eta, int64_t n_tok, float* d_dW1, float* d_dW2,
