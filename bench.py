@@ -100,8 +100,8 @@ def tokens_per_step(w: li.Workload) -> int:
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one
 # full-size launch of the fused gradient kernel on the million-token layer,
-# from a one-pass ncu capture (summary: profiles/k_grad_tc_million_token_set.md).
-# It describes the kernel source it was taken on, identified by its hash.
+# from an ncu capture of that kernel. It describes the kernel source it was
+# taken on, identified by its hash.
 GRAD_TRAFFIC = {"workload": 5, "bytes": 4454414336 + 134320896, "kernel_source": "k_tc_grad.cu",
                 "sha256_prefix": "83ae3cd43ad83ce0"}
 
@@ -116,6 +116,15 @@ def measured_traffic(w: li.Workload, reduced: bool):
     except OSError:
         return None
     return GRAD_TRAFFIC["bytes"] if sha.startswith(GRAD_TRAFFIC["sha256_prefix"]) else None
+
+
+FP64_TFLOPS = 1.25          # B300 dense fp64, nominal
+BF16_MAC_PER_CLK_SM = 4096  # dense bf16 tensor-core MACs per clock per SM
+
+
+def dense_bf16_tflops(sm_mhz: float, sms: int = 148) -> float:
+    """Dense bf16 tensor rate at a given SM clock: SMs x 4,096 MACs x 2 FLOP."""
+    return sms * BF16_MAC_PER_CLK_SM * 2 * sm_mhz * 1e6 / 1e12
 
 
 def peaks():
@@ -443,15 +452,24 @@ def main():
         peak, bound, note = pk["bf16_tflops"], "tensor", f"dense bf16 burst, {pk_src}"
         kernel = "k_grad_tc" if w.d == 128 else "k_fwdbwd_tc + k_wgrad_tc"
     else:
-        # CUDA-core fp32 FMA: 148 SMs x 128 FMA/clk x 2 FLOP x max SM clock
-        peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
-        bound, note = "alu", "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"
+        # the fp32-io path computes in fp64 on the CUDA cores: B300's nominal
+        # dense fp64 rate
+        peak = FP64_TFLOPS
+        bound, note = "alu", "fp64 FMA (the fp32-io path computes in fp64): nominal 1.25 TFLOP/s"
         kernel = "k_grad_simt"
     roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
             "frac": achieved / peak,
             "traffic": measured_traffic(w, reduced), "traffic_unit": "bytes per launch", "kernel": kernel,
             "peak_source": note, "ms_per_launch": grad_ms, "flop_per_launch": grad_flop,
             "launches_per_call": grad["launches"] / max(1, grad["calls"])}
+    if bound == "tensor":
+        # the same rate against the tensor cores' own dense rate (4,096 bf16
+        # MACs per clock per SM) at the maximum and at the sampled SM clock
+        for key, mhz in (("max_clock", pk.get("sm_max_mhz", 2032.0)), ("median_clock", (ck or {}).get("sm_mhz"))):
+            if mhz:
+                p_clk = dense_bf16_tflops(mhz)
+                roof["peak_dense_" + key] = p_clk
+                roof["frac_dense_" + key] = achieved / p_clk
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
