@@ -60,6 +60,10 @@ constexpr uint64_t WAIT_NS = 2000000000ull;
 
 struct NsArgs {
     float* g[3];      // gradients in place: W1 [BH,dh,d], W2 [BH,d,dh], W3 [BH,dh,d]
+    const float* part;    // split-K partial slots [slots][nmat][BH][d*dh] (read when slots > 0)
+    int slots;
+    size_t mat;           // BH * d * dh
+    int nmat;
     int BH, d, dh, n, steps;
     float a, b, c;
     int* status;
@@ -137,6 +141,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     // is G[j][row] when G is stored tall (a warp's 32 rows read 32
     // consecutive words), else G[row][j] (the thread reads 128 contiguous bytes)
     auto load32 = [&](int j0, float* x) {
+        if (a.slots > 0) {
+            // the split-K partial sums of this matrix, added in slot order
+            const float* P0 = a.part + (size_t)which * a.mat + (size_t)bh * a.d * a.dh;
+            const size_t stride = (size_t)a.nmat * a.mat;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) x[t] = 0.f;
+            for (int sl = 0; sl < a.slots; ++sl) {
+                const float* P = P0 + (size_t)sl * stride;
+                if (tr) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) x[t] += P[(size_t)(j0 + t) * cols + row];
+                } else {
+                    const float4* gp = reinterpret_cast<const float4*>(P + (size_t)row * cols + j0);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const float4 v = gp[t];
+                        x[4 * t] += v.x; x[4 * t + 1] += v.y; x[4 * t + 2] += v.z; x[4 * t + 3] += v.w;
+                    }
+                }
+            }
+            return;
+        }
         if (tr) {
 #pragma unroll
             for (int t = 0; t < 32; ++t) x[t] = G[(size_t)(j0 + t) * cols + row];
@@ -459,9 +485,13 @@ bool ns_tc_supported(const lact_state* st) {
     return st->cfg.io_dtype == LACT_BF16 && m == M && n <= NMAX && n % 128 == 0;
 }
 
-cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s) {
+cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], int slots, cudaStream_t s) {
     NsArgs a;
     for (int m = 0; m < 3; ++m) a.g[m] = static_cast<float*>(g[m]);
+    a.part = static_cast<const float*>(st->partial);
+    a.slots = slots;
+    a.mat = (size_t)st->BH * st->cfg.d * st->cfg.dh;
+    a.nmat = st->nmat;
     a.BH = st->BH;
     a.d = st->cfg.d;
     a.dh = st->cfg.dh;

@@ -139,8 +139,12 @@ static lact_status do_apply(lact_state* st, TokView q, void* o, cudaStream_t s) 
 }
 
 // Chunk gradient of tokens [k.t0, k.t0 + k.n) into out[] (accumulate: add to it).
+// With `deferred` non-null, a Muon step that follows may take the split-K sum
+// over: when the tensor-core Newton-Schulz will run and the partial slots are
+// few, the reduction is skipped and *deferred holds their count (else 0).
 static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* eta, bool accumulate,
-                           void* const out[3], cudaStream_t s) {
+                           void* const out[3], cudaStream_t s, int* deferred = nullptr) {
+    if (deferred) *deferred = 0;
     if (k.n == 0) {
         if (!accumulate) {
             const size_t bytes = (size_t)st->BH * st->cfg.d * st->cfg.dh * st->rsize;
@@ -172,6 +176,11 @@ static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* et
         t.done();
         if (e != cudaSuccess) return LACT_ERR_CUDA;
     }
+    if (deferred && !accumulate && out == st->dW && st->cfg.opt == LACT_OPT_MUON && ns_tc_supported(st) &&
+        (grad_tc_supported(st) || (st->nmat == 1 && lin_tc_supported(st))) && slots >= 1 && slots <= kNsFusedSlots) {
+        *deferred = slots;   // Newton-Schulz adds the slots while it reads them
+        return LACT_OK;
+    }
     PhaseTimer t(st, LACT_PHASE_REDUCE, s);
     cudaError_t e = launch_reduce(st, slots, accumulate, out, s);
     t.done();
@@ -179,11 +188,13 @@ static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* et
 }
 
 // Optimiser step + renorm from the gradient in g[] (Muon overwrites g[]).
-static lact_status do_step(lact_state* st, void* const g[3], cudaStream_t s) {
+// slots > 0: the gradient is still in that many split-K slots (do_grad's
+// `deferred`), summed by Newton-Schulz as it reads them.
+static lact_status do_step(lact_state* st, void* const g[3], cudaStream_t s, int slots = 0) {
     double scale = -1.0;
     if (st->cfg.opt == LACT_OPT_MUON) {
         PhaseTimer t(st, LACT_PHASE_NS, s);
-        cudaError_t e = ns_tc_supported(st) ? launch_ns_tc(st, g, s) : launch_newton_schulz(st, g, s);
+        cudaError_t e = ns_tc_supported(st) ? launch_ns_tc(st, g, slots, s) : launch_newton_schulz(st, g, s);
         t.done();
         if (e != cudaSuccess) return LACT_ERR_CUDA;
         scale = -st->cfg.muon_lr;
@@ -313,9 +324,10 @@ lact_status lact_chunk_update(lact_state* st, const void* d_k, const void* d_v, 
     lact_status r = check_update(st, d_k, d_v, d_eta, n_tok);
     if (r != LACT_OK) return r;
     st->last_stream = s;
-    r = do_grad(st, TokView{d_k, n_tok, 0, n_tok}, TokView{d_v, n_tok, 0, n_tok}, d_eta, false, st->dW, s);
+    int deferred = 0;
+    r = do_grad(st, TokView{d_k, n_tok, 0, n_tok}, TokView{d_v, n_tok, 0, n_tok}, d_eta, false, st->dW, s, &deferred);
     if (r != LACT_OK) return r;
-    return do_step(st, st->dW, s);
+    return do_step(st, st->dW, s, deferred);
 }
 
 lact_status lact_chunk_gradient(lact_state* st, const void* d_k, const void* d_v, const float* d_eta,
@@ -370,10 +382,11 @@ lact_status lact_sequence(lact_state* st, lact_order order, const void* d_q, int
             r = do_apply(st, TokView{d_q, n_q, t0, n}, d_o, st->side);
             if (r != LACT_OK) return r;
             if (cudaEventRecord(st->ev_join, st->side) != cudaSuccess) return LACT_ERR_CUDA;
-            r = do_grad(st, TokView{d_k, n_kv, t0, n}, TokView{d_v, n_kv, t0, n}, d_eta, false, st->dW, s);
+            int deferred = 0;
+            r = do_grad(st, TokView{d_k, n_kv, t0, n}, TokView{d_v, n_kv, t0, n}, d_eta, false, st->dW, s, &deferred);
             if (r != LACT_OK) return r;
             if (cudaStreamWaitEvent(s, st->ev_join, 0) != cudaSuccess) return LACT_ERR_CUDA;
-            r = do_step(st, st->dW, s);
+            r = do_step(st, st->dW, s, deferred);
             if (r != LACT_OK) return r;
         }
         return LACT_OK;
@@ -382,12 +395,14 @@ lact_status lact_sequence(lact_state* st, lact_order order, const void* d_q, int
     if (n_kv == 0) {
         r = do_grad(st, TokView{d_k, n_kv, 0, 0}, TokView{d_v, n_kv, 0, 0}, d_eta, false, st->dW, s);
     }
+    int deferred = 0;   // (one slice only: several are summed into dW first)
     for (int64_t t0 = 0; t0 < n_kv && r == LACT_OK; t0 += chunk) {
         const int64_t n = n_kv - t0 < chunk ? n_kv - t0 : chunk;
-        r = do_grad(st, TokView{d_k, n_kv, t0, n}, TokView{d_v, n_kv, t0, n}, d_eta, t0 > 0, st->dW, s);
+        r = do_grad(st, TokView{d_k, n_kv, t0, n}, TokView{d_v, n_kv, t0, n}, d_eta, t0 > 0, st->dW, s,
+                    n == n_kv ? &deferred : nullptr);
     }
     if (r != LACT_OK) return r;
-    r = do_step(st, st->dW, s);
+    r = do_step(st, st->dW, s, deferred);
     if (r != LACT_OK) return r;
     return do_apply(st, TokView{d_q, n_q, 0, n_q}, d_o, s);
 }

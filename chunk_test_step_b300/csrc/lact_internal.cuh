@@ -166,7 +166,12 @@ bool grad_tc_supported(const lact_state* st);
 cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots_used,
                            cudaStream_t s);
 bool ns_tc_supported(const lact_state* st);
-cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], cudaStream_t s);
+// Newton-Schulz in place on g[]. With slots > 0 the gradient is not in g[]
+// yet: the kernel adds the split-K partial slots 0 .. slots-1 (in that order,
+// as launch_reduce does) while it reads them, and writes its result to g[].
+cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], int slots, cudaStream_t s);
+// Most split-K slots Newton-Schulz adds up itself (more go through launch_reduce).
+constexpr int kNsFusedSlots = 4;
 bool apply_tc_supported(const lact_state* st);
 cudaError_t launch_apply_tc(const lact_state* st, TokView q, void* o, cudaStream_t s);
 // Head dim 128: two 128-query tiles per CTA sharing every streamed weight block.

@@ -173,10 +173,10 @@ def test_two_slices_on_the_gpu_match_the_whole_chunk(num):
     want = [np.zeros_like(g) for g in got]
     for b in range(w.B):
         for h in range(w.H):
-            Wf = O.chunk_update(tuple(x[h].astype(np.float64) for x in mats), li.as_f64(inp.k[b, h]),
-                                li.as_f64(inp.v[b, h]), inp.eta[b, h].astype(np.float64), w.opt,
-                                lr=w.muon_lr, ns_steps=w.ns_steps,
-                                mom=O.zero_velocity(mats) if w.opt == "momentum" else None, beta=w.momentum)
+            W0h = tuple(x[h].astype(np.float64) for x in mats)
+            Wf = O.chunk_update(W0h, li.as_f64(inp.k[b, h]), li.as_f64(inp.v[b, h]),
+                                inp.eta[b, h].astype(np.float64), w.opt, lr=w.muon_lr, ns_steps=w.ns_steps,
+                                mom=O.zero_velocity(W0h) if w.opt == "momentum" else None, beta=w.momentum)
             for m in range(len(got)):
                 want[m][b, h] = Wf[m]
     for m in range(len(got)):

@@ -347,9 +347,12 @@ def test_profiling_counts_phases():
     layer.sequence(L.LACT_SET_UPDATE_THEN_APPLY, q, k, v, e, w.chunk)
     prof = L.lact_get_profile(layer.handle)
     n1 = L.lact_launch_count()
-    assert all(prof[p]["calls"] == 1 for p in ("apply", "grad", "reduce", "ns", "update"))
+    assert all(prof[p]["calls"] == 1 for p in ("apply", "grad", "ns", "update"))
+    # the split-K sum is its own phase, or (few token splits before a Muon
+    # step) done by Newton-Schulz as it reads the partial sums
+    assert prof["reduce"]["calls"] in (0, 1)
     assert sum(prof[p]["launches"] for p in prof) == n1 - n0
-    assert all(prof[p]["ms"] > 0 for p in prof)
+    assert all(prof[p]["ms"] > 0 for p in prof if prof[p]["calls"] > 0)
 
 
 @pytest.mark.parametrize("num", [2, 4, 5, 7, 8, 10])
@@ -476,3 +479,28 @@ def test_sequence_replayed_from_a_cuda_graph_matches_direct_calls(num):
     errs = compare(w, tuple(None if x is None else to_host_f64(x) for x in replay + [None] * (4 - len(replay))),
                    O.run_workload(w, inp), "graph_replay")
     assert max(errs.values()) < TOL[w.dtype], errs
+
+
+@pytest.mark.parametrize("num,n", [(4, 5000 + 13), (8, 4096), (5, 8192 + 77), (10, 3000)])
+def test_update_equals_gradient_then_apply_gradient(num, n):
+    # One update (gradient, its split-K sum, Muon step, renorm) against the
+    # same done as two calls: lact_chunk_gradient (the sum by the reduction
+    # kernel) then lact_apply_gradient. With few token splits the update lets
+    # Newton-Schulz add the partial sums as it reads them, in the reduction's
+    # order, so the two agree bit for bit either way.
+    torch = _torch()
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[num].with_tokens(n, seed=li.WORKLOADS[num].seed + 7000)
+    inp = li.make_inputs(w)
+    k, v, e = to_device(inp.k), to_device(inp.v), to_device(inp.eta)
+    one = _layer(w, inp, max_chunk=n)
+    L.lact_chunk_update(one.handle, k, v, e, n)
+    two = _layer(w, inp, max_chunk=n)
+    shapes = ((w.d, w.d),) if w.memory == "linear" else ((w.dh, w.d), (w.d, w.dh), (w.dh, w.d))
+    g = [torch.empty(w.B, w.H, *s, device="cuda") for s in shapes] + [None] * (3 - len(shapes))
+    L.lact_chunk_gradient(two.handle, k, v, e, n, *g)
+    L.lact_apply_gradient(two.handle, *g)
+    a, b = one.weights(), two.weights()
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert (x is None and y is None) or torch.equal(x, y)
