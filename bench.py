@@ -100,9 +100,11 @@ def tokens_per_step(w: li.Workload) -> int:
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one
 # full-size launch of the fused gradient kernel on the million-token layer,
-# from an ncu capture of that kernel. It describes the kernel source it was
-# taken on, identified by its hash.
-GRAD_TRAFFIC = {"workload": 5, "bytes": 4454414336 + 134320896, "kernel_source": "k_tc_grad.cu",
+# scaled from an ncu capture of a reduced launch (131,072 tokens per head, 9
+# token splits): reads (K, V, eta) grow with the tokens (x 8), writes (the
+# split-K partial sums) with the splits (23 at full size). It describes the
+# kernel source it was taken on, identified by its hash.
+GRAD_TRAFFIC = {"workload": 5, "bytes": 560205824 * 8 + 46391808 * 23 // 9, "kernel_source": "k_tc_grad.cu",
                 "sha256_prefix": "83ae3cd43ad83ce0"}
 
 
