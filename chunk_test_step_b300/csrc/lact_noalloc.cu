@@ -30,27 +30,29 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mutex;
-int g_num_sms[kMaxDevices] = {};   // SM count per device (a property of the device, kept)
+void* g_scratch_addr[kMaxDevices] = {};   // device address of g_scratch, per device
+int g_num_sms[kMaxDevices] = {};
 
 // Device address of g_scratch on the current device (host code may not use
-// g_scratch's name as a device pointer). Looked up on every call, so that a
-// context torn down and recreated (cudaDeviceReset) never leaves a stale
-// address behind; once this file's module is loaded on the device the lookup
-// allocates nothing. The module itself (with the array) is loaded by the
-// first lookup on each device when CUDA loads modules lazily, which is an
-// allocation: hence the warm-up call the header asks for.
+// g_scratch's name as a device pointer), looked up once per device by the
+// first call made with that device current, and kept. When CUDA loads
+// modules lazily that first lookup also loads this file's module, array
+// included, which allocates: hence the warm-up call the header asks for. The
+// kept address belongs to the device's current context: after
+// cudaDeviceReset the library must not be used again in the process.
 lact_status scratch_for_current_device(float** out, int* num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LACT_ERR_CUDA;
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return LACT_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_num_sms[dev]) {
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return LACT_ERR_CUDA;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LACT_ERR_CUDA;
+        g_scratch_addr[dev] = p;
         g_num_sms[dev] = sms;
     }
-    *out = static_cast<float*>(p);
+    *out = static_cast<float*>(g_scratch_addr[dev]);
     *num_sms = g_num_sms[dev];
     return LACT_OK;
 }

@@ -206,13 +206,15 @@ lact_status lact_import_state(lact_state* st, const void* d_src, size_t bytes, c
  * device memory inside this library, held by every GPU that loads it until
  * the process exits; one split slot takes 12*B*H*d*dh bytes, and a problem
  * whose slot does not fit returns LACT_ERR_UNSUPPORTED before anything runs.
- * Each call looks up that array's device address. CUDA loads a library's
- * device code lazily by default, and the first call on each device is what
- * loads the part holding the array: that load allocates device memory (the
- * array, the code) and may synchronise. So make one warm-up call per device
- * outside any path that must not allocate, and before any stream capture (or
- * run the process with CUDA_MODULE_LOADING=EAGER); later calls allocate
- * nothing. All calls share the array: two calls that may overlap on the GPU
+ * The first call on each device (with that device current) looks up the
+ * array's device address and keeps it. CUDA loads a library's device code
+ * lazily by default, and that first lookup is what loads the part holding
+ * the array: the load allocates device memory (the array, the code) and may
+ * synchronise. So make one warm-up call per device outside any path that must
+ * not allocate, and before any stream capture (or run the process with
+ * CUDA_MODULE_LOADING=EAGER); later calls allocate nothing. The kept address
+ * belongs to the device's context: do not use this call again after
+ * cudaDeviceReset. All calls share the array: two calls that may overlap on the GPU
  * (other streams, other host threads) race, so order them on one stream.
  * Nothing in it needs clearing: each call overwrites what it reads. Calls no
  * cudaMalloc, cudaFree or other allocating routine. */
