@@ -142,23 +142,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     // consecutive words), else G[row][j] (the thread reads 128 contiguous bytes)
     auto load32 = [&](int j0, float* x) {
         if (a.slots > 0) {
-            // the split-K partial sums of this matrix, added in slot order
+            // the split-K partial sums of this matrix, added in slot order;
+            // every slot's loads are issued before the first add
             const float* P0 = a.part + (size_t)which * a.mat + (size_t)bh * a.d * a.dh;
             const size_t stride = (size_t)a.nmat * a.mat;
+            float y[2][32];
 #pragma unroll
             for (int t = 0; t < 32; ++t) x[t] = 0.f;
-            for (int sl = 0; sl < a.slots; ++sl) {
-                const float* P = P0 + (size_t)sl * stride;
-                if (tr) {
+            for (int s0 = 0; s0 < a.slots; s0 += 2) {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) x[t] += P[(size_t)(j0 + t) * cols + row];
-                } else {
-                    const float4* gp = reinterpret_cast<const float4*>(P + (size_t)row * cols + j0);
+            for (int u = 0; u < 2; ++u) {
+                const int sl = s0 + u;
+                if (sl < a.slots) {
+                    const float* P = P0 + (size_t)sl * stride;
+                    if (tr) {
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const float4 v = gp[t];
-                        x[4 * t] += v.x; x[4 * t + 1] += v.y; x[4 * t + 2] += v.z; x[4 * t + 3] += v.w;
+                        for (int t = 0; t < 32; ++t) y[u][t] = P[(size_t)(j0 + t) * cols + row];
+                    } else {
+                        const float4* gp = reinterpret_cast<const float4*>(P + (size_t)row * cols + j0);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) {
+                            const float4 v = gp[t];
+                            y[u][4 * t] = v.x; y[u][4 * t + 1] = v.y; y[u][4 * t + 2] = v.z; y[u][4 * t + 3] = v.w;
+                        }
                     }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (s0 + u < a.slots) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) x[t] += y[u][t];
                 }
             }
             return;
@@ -286,9 +300,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     };
     // "My A GEMM is done with Xb": thread 0 (which saw the MMA complete)
     // arrives on the barrier of every CTA of the cluster.
+    // (Relaxed: the A GEMM's reads of Xb have completed, as the MMA barrier
+    // showed; nothing written by this thread needs ordering before the
+    // other CTAs overwrite Xb.)
     auto arrive_a_done = [&]() {
         if (tid == 0)
-            for (int r = 0; r < cs; ++r) mbar_arrive_cluster(mapa_shared(bar_a, (uint32_t)r));
+            for (int r = 0; r < cs; ++r)
+                asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
+                             ::"r"(mapa_shared(bar_a, (uint32_t)r)) : "memory");
     };
     // Bounded wait on a local cluster barrier, made block-uniform.
     auto cluster_wait = [&](uint32_t b, uint32_t parity) -> bool {
