@@ -59,7 +59,10 @@ __device__ __forceinline__ void store_vec(double* p, const double* v, int n) {
     for (int k = 0; k < n; ++k) p[k] = v[k];
 }
 
-template <typename R, int VEC>
+// MAXV: pieces of 32*VEC elements of the longest row, fixed at compile time so
+// the row stays in registers (sized to the shape: fewer registers, more warps
+// resident, for the common row lengths up to 512).
+template <typename R, int VEC, int MAXV>
 __global__ void __launch_bounds__(256) k_update_renorm(UpdArgs<R> a) {
     pdl_wait();
     const int lane = threadIdx.x & 31;
@@ -76,8 +79,7 @@ __global__ void __launch_bounds__(256) k_update_renorm(UpdArgs<R> a) {
     R* w = a.W[m] + row * len;
     const R* dv = a.D[m] + row * len;
     R* mo = a.Mo[m] ? a.Mo[m] + row * len : nullptr;
-    // Pass 1: both norms. Rows are at most 1024 long: keep them in registers.
-    constexpr int MAXV = 1024 / (32 * VEC);
+    // Pass 1: both norms, the row kept in registers.
     R wt[MAXV][VEC];
     R n0 = 0, n1 = 0;
 #pragma unroll
@@ -168,8 +170,13 @@ cudaError_t update_t(const lact_state* st, const void* const g[3], double scale,
     const int64_t rows = (int64_t)st->BH * (a.rows[0] + a.rows[1] + a.rows[2]);
     const int blocks = (int)((rows * 32 + 255) / 256);
     // every row length here is a multiple of 32; float4 when a multiple of 128
-    if (sizeof(R) == 4 && d % 128 == 0 && dh % 128 == 0) launch_pdl(k_update_renorm<R, 4>, blocks, 256, 0, s, a);
-    else launch_pdl(k_update_renorm<R, 1>, blocks, 256, 0, s, a);
+    const int maxlen = d > dh ? d : dh;
+    if (sizeof(R) == 4 && d % 128 == 0 && dh % 128 == 0) {
+        if (maxlen <= 512) launch_pdl(k_update_renorm<R, 4, 4>, blocks, 256, 0, s, a);
+        else launch_pdl(k_update_renorm<R, 4, 8>, blocks, 256, 0, s, a);
+    } else {
+        launch_pdl(k_update_renorm<R, 1, 32>, blocks, 256, 0, s, a);
+    }
     g_launches++;
     return cudaGetLastError();
 }
