@@ -28,6 +28,11 @@
 // cluster-wide handshake, "every CTA's A GEMM has finished reading Xb",
 // comes before anyone overwrites it.
 //
+// G is either the summed gradient or, when the caller skipped the split-K
+// reduction, its partial slots: each CTA then adds its columns' slots in slot
+// order as it reads them (the reduction kernel's order, so the result is the
+// same bit for bit).
+//
 // 256 threads: thread = row of X (TMEM lane) and half of the CTA's columns;
 // thread 0 also issues the MMAs. Every mbarrier wait is bounded and its
 // outcome made block-uniform; the hardware cluster barrier is used only at

@@ -52,7 +52,7 @@ def _free_port() -> int:
         return s.getsockname()[1]
 
 
-def _cp_worker(rank, world, port, opt, memory, out):
+def _cp_worker(rank, world, port, opt, memory, out, n=1000):
     sys.path.insert(0, ROOT)
     import torch
     import torch.distributed as dist
@@ -64,7 +64,7 @@ def _cp_worker(rank, world, port, opt, memory, out):
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
     try:
         d, dh = 16, (16 if memory == "linear" else 32)
-        w = li.Workload(0, "cp-tiny", 1, 2, d, dh, "f32", "set", opt, 1000, 40, 1000, 4321, memory=memory)
+        w = li.Workload(0, "cp-tiny", 1, 2, d, dh, "f32", "set", opt, n, 40, n, 4321, memory=memory)
         inp = li.make_inputs(w)
         lin = memory == "linear"
         Wh = [inp.W1] if lin else [inp.W1, inp.W2, inp.W3]
@@ -116,13 +116,16 @@ def _cp_worker(rank, world, port, opt, memory, out):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("opt,memory", [("gd", "swiglu"), ("muon", "swiglu"), ("momentum", "swiglu"),
-                                        ("muon", "linear")])
-def test_two_gloo_ranks_sum_slice_gradients_into_the_whole_chunk_update(opt, memory):
+@pytest.mark.parametrize("opt,memory,world,n", [("gd", "swiglu", 2, 1000), ("muon", "swiglu", 2, 1000),
+                                                ("momentum", "swiglu", 2, 1000), ("muon", "linear", 2, 1000),
+                                                ("gd", "swiglu", 3, 300)])
+def test_gloo_ranks_sum_slice_gradients_into_the_whole_chunk_update(opt, memory, world, n):
+    # (three ranks on 300 tokens: slices of 128, 128 and 44 tokens; the
+    # uneven, ragged last slice still sums to the whole chunk)
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_cp_worker, args=(r, 2, port, opt, memory, q)) for r in range(2)]
+    procs = [ctx.Process(target=_cp_worker, args=(r, world, port, opt, memory, q, n)) for r in range(world)]
     for p in procs:
         p.start()
     res = [q.get(timeout=240) for _ in procs]
@@ -187,3 +190,63 @@ def test_two_slices_on_the_gpu_match_the_whole_chunk(num):
     assert max(dW.values()) < dw_tol(w, False), dW
     for layer, _ in ranks:
         layer.close()
+
+
+def _cp_empty_worker(rank, world, port, out):
+    # more ranks than tiles: the ranks past the last tile hold an empty slice
+    # and contribute zeros; everyone still ends with the whole chunk's update
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+
+    import lact_inputs as li
+    from chunk_test_step_b300 import lact as L
+    from chunk_test_step_b300.context_parallel import ContextParallelUpdate
+    from oracle import lact_oracle as O
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        d, dh, n = 16, 32, 150                          # 2 tiles of 128 tokens over 4 ranks
+        w = li.Workload(0, "cp-empty", 1, 1, d, dh, "f32", "set", "gd", n, 8, n, 4322)
+        inp = li.make_inputs(w)
+        W = [x[0].astype(np.float64) for x in (inp.W1, inp.W2, inp.W3)]
+
+        def gradient(k, v, eta, n_local, grads, stream=None):
+            if n_local == 0:
+                for g in grads[:3]:
+                    g.zero_()
+                return
+            for m, gm in enumerate(O.chunk_gradient(*W, li.as_f64(k[0, 0]), li.as_f64(v[0, 0]),
+                                                    eta[0, 0].astype(np.float64))):
+                grads[m][0, 0] = torch.from_numpy(gm)
+
+        result = {}
+
+        def step(grads, stream=None):
+            result["W"] = [O.renorm_update(Wm, -grads[m][0, 0].double().numpy()) for m, Wm in enumerate(W)]
+
+        cfg = L.make_config(1, 1, d, dh, "f32", "gd", max_chunk=n)
+        cp = ContextParallelUpdate(SimpleNamespace(cfg=cfg, handle=None), device="cpu", gradient=gradient, step=step,
+                                   dtype=torch.float64)
+        t0, t1 = cp.slice(n)
+        cp.update(inp.k[:, :, t0:t1], inp.v[:, :, t0:t1], inp.eta[:, :, t0:t1], t1 - t0)
+        want = O.chunk_update(tuple(W), li.as_f64(inp.k[0, 0]), li.as_f64(inp.v[0, 0]),
+                              inp.eta[0, 0].astype(np.float64), "gd")
+        err = max(float(np.linalg.norm(a - b) / np.linalg.norm(b)) for a, b in zip(result["W"], want))
+        out.put((rank, t1 - t0, err))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_ranks_beyond_the_last_tile_contribute_nothing():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_cp_empty_worker, args=(r, 4, port, q)) for r in range(4)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=240) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    assert [r[1] for r in res] == [128, 22, 0, 0]
+    assert all(r[2] < 1e-12 for r in res), res
