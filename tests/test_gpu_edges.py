@@ -9,6 +9,10 @@ through the C ABI, against the fp64 oracle.
   both io dtypes, through whichever kernels serve them (tensor-core or
   CUDA-core gradient and readout, Newton-Schulz on the tensor cores or, for
   shapes it does not serve, on the CUDA cores).
+* A set-order call with no update tokens reads the initial memory and leaves
+  it bit for bit; one with no queries still updates.
+* Two states driven on two streams at once give what they give one after the
+  other (each state owns its workspace and side stream).
 """
 import dataclasses
 
@@ -104,3 +108,80 @@ def test_configuration_corners_match_oracle(d, dh, dtype, opt):
     assert max(errs.values()) < TOL[w.dtype], errs
     dW = compare_change(w, initial_weights(w, inp), got[1:], want[1:], exact_gradient=False, test="corner")
     assert max(dW.values()) < dw_tol(w, False), dW
+
+
+@pytest.mark.parametrize("num", [4, 10, 3])
+def test_set_call_with_no_update_tokens_reads_the_initial_memory(num):
+    # lact_sequence in the set order with n_kv = 0: the (empty) update leaves
+    # W bit for bit, and the queries read the initial fast weights
+    import torch
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[num].with_tokens(0, n_q=300, chunk=1, seed=li.WORKLOADS[num].seed + 8200)
+    w = dataclasses.replace(w, order="set")
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp, max_chunk=1)
+    before = [None if x is None else x.clone() for x in layer.weights()]
+    q = to_device(inp.q)
+    z = torch.zeros(16, device="cuda")
+    o = torch.empty_like(q)
+    L.lact_sequence(layer.handle, L.LACT_SET_UPDATE_THEN_APPLY, q, w.n_q, z, z, z, 0, 1, o)
+    after = layer.weights()
+    torch.cuda.synchronize()
+    assert L.lact_sync_status(layer.handle) == L.LACT_OK
+    for x, y in zip(before, after):
+        assert (x is None and y is None) or torch.equal(x, y)
+    got = to_host_f64(o)
+    mats = (inp.W1,) if w.memory == "linear" else (inp.W1, inp.W2, inp.W3)
+    for b in range(w.B):
+        for h in range(w.H):
+            want = O.memory_apply(tuple(x[h].astype(np.float64) for x in mats), li.as_f64(inp.q[b, h]))
+            err = np.linalg.norm(got[b, h] - want) / np.linalg.norm(want)
+            assert err < TOL[w.dtype], (b, h, err)
+
+
+def test_set_call_with_no_queries_still_updates():
+    import torch
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[4].with_tokens(1000 + 3, n_q=0, seed=li.WORKLOADS[4].seed + 8300)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp, max_chunk=w.n_kv)
+    k, v, e = to_device(inp.k), to_device(inp.v), to_device(inp.eta)
+    z = torch.zeros(16, device="cuda")
+    L.lact_sequence(layer.handle, L.LACT_SET_UPDATE_THEN_APPLY, z, 0, k, v, e, w.n_kv, w.n_kv, z)
+    got = [to_host_f64(x) for x in layer.weights()]
+    torch.cuda.synchronize()
+    assert L.lact_sync_status(layer.handle) == L.LACT_OK
+    want = O.run_workload(w, inp)
+    errs = compare(w, (None,) + tuple(got), (None,) + tuple(want[1:]), "no_queries")
+    assert max(errs.values()) < TOL[w.dtype], errs
+
+
+def test_two_states_on_two_streams_run_independently():
+    # two layers, each on its own stream, launched interleaved: the results
+    # equal those of the same calls made one after the other
+    import torch
+    from chunk_test_step_b300 import lact as L
+    ws = [li.WORKLOADS[8].with_tokens(4096 + 11, seed=li.WORKLOADS[8].seed + 8400),
+          li.WORKLOADS[2].with_tokens(2048 + 5, seed=li.WORKLOADS[2].seed + 8400)]
+    inps = [li.make_inputs(w) for w in ws]
+
+    def run(concurrent):
+        layers = [_layer(w, inp) for w, inp in zip(ws, inps)]
+        ios = [tuple(to_device(x) for x in (inp.q, inp.k, inp.v, inp.eta)) for inp in inps]
+        outs = [torch.empty_like(io[0]) for io in ios]
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()] if concurrent else [torch.cuda.current_stream()] * 2
+        torch.cuda.synchronize()
+        for i, (w, layer, (q, k, v, e), o, s) in enumerate(zip(ws, layers, ios, outs, streams)):
+            L.lact_sequence(layer.handle, L.LACT_CAUSAL_APPLY_THEN_UPDATE, q, w.n_q, k, v, e, w.n_kv, w.chunk, o, s)
+        torch.cuda.synchronize()
+        res = [[o.clone()] + [x.clone() for x in layer.weights() if x is not None] for layer, o in zip(layers, outs)]
+        torch.cuda.synchronize()
+        for layer in layers:
+            assert L.lact_sync_status(layer.handle) == L.LACT_OK
+            layer.close()
+        return res
+
+    seq, conc = run(False), run(True)
+    for a, b in zip(seq, conc):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
