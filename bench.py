@@ -52,6 +52,10 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     # time direct lact_sequence calls instead of a CUDA-graph replay of one
     p.add_argument("--no-graph", action="store_true")
+    # one update chunk spread over the ranks by tokens (each rank's slice
+    # gradient, one all-reduce of the gradients, the same update everywhere;
+    # queries split likewise): strong scaling of one layer call. Set order only.
+    p.add_argument("--context-parallel", action="store_true")
     # smaller token counts of the same layer (for profiler captures of a small case)
     p.add_argument("--update-tokens", type=int, default=None)
     p.add_argument("--query-tokens", type=int, default=None)
@@ -289,6 +293,133 @@ def run_reference(args, w):
     return 0
 
 
+def run_context_parallel(args, w):
+    """One layer call of a set-order workload spread over the ranks by tokens.
+
+    Rank r holds tokens token_range(n_kv, r, N) of the update chunk and
+    token_range(n_q, r, N) of the queries (both [B, H, slice, d]); per step it
+    computes its slice gradient, the ranks all-reduce the gradients (NCCL),
+    every rank applies the same update, then reads its queries. The job's
+    time is the slowest rank's; `value` is the whole layer's tokens over it
+    (strong scaling: the work is one call whatever N is)."""
+    import torch
+    from chunk_test_step_b300 import lact as L
+    from chunk_test_step_b300.context_parallel import ContextParallelUpdate, token_range
+    if w.order != "set":
+        raise SystemExit("--context-parallel serves the set order (one update chunk, then queries)")
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    inp = li.make_inputs(w)
+    t0, t1 = token_range(w.n_kv, rank, world)
+    q0, q1 = token_range(w.n_q, rank, world)
+    hq, hk, hv, he = pinned_inputs(w, li.Inputs(np.ascontiguousarray(inp.q[:, :, q0:q1]),
+                                                np.ascontiguousarray(inp.k[:, :, t0:t1]),
+                                                np.ascontiguousarray(inp.v[:, :, t0:t1]),
+                                                np.ascontiguousarray(inp.eta[:, :, t0:t1]), None, None, None))
+    q, k, v, e = (x.to(dev) for x in (hq, hk, hv, he))
+    n_loc, nq_loc = t1 - t0, q1 - q0
+    W1, W2, W3 = (None if x is None else torch.from_numpy(x).to(dev) for x in (inp.W1, inp.W2, inp.W3))
+    del inp
+    cfg = L.make_config(w.B, w.H, w.d, w.dh, w.dtype, w.opt, max_chunk=max(1, n_loc), ns_steps=w.ns_steps,
+                        ns_a=w.ns_a, ns_b=w.ns_b, ns_c=w.ns_c, muon_lr=w.muon_lr, momentum=w.momentum,
+                        memory=w.memory)
+    layer = L.LactLayer(cfg, W1, W2, W3, device=dev)
+    cp = ContextParallelUpdate(layer, group=None if pg is None else pg.group.WORLD)
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        cp.update(k, v, e, n_loc, stream)
+        L.lact_chunk_apply(layer.handle, q, nq_loc, o, stream)
+
+    def barrier():
+        if pg:
+            pg.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    def timed(run, n):
+        barrier()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            run()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        return a.elapsed_time(b)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)
+    n0 = L.lact_launch_count()
+    ms_step = max_over_ranks(timed(step, args.steps), pg, dev) / args.steps
+    launches = L.lact_launch_count() - n0
+    ck = clocks.stop()
+    L.lact_set_profiling(layer.handle, True)
+    timed(step, args.steps)
+    prof = L.lact_get_profile(layer.handle)
+    L.lact_set_profiling(layer.handle, False)
+
+    def e2e_step():
+        for d_, h_ in ((q, hq), (k, hk), (v, hv), (e, he)):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    e2e_ms = max_over_ranks(timed(e2e_step, args.e2e_steps), pg, dev) / args.e2e_steps
+    st = L.lact_sync_status(layer.handle)
+    if st != L.LACT_OK:
+        raise RuntimeError(f"device status after the timed region: {L.lact_status_str(st)}")
+
+    pk, pk_src = peaks()
+    grad = prof["grad"]
+    grad_ms = grad["ms"] / max(1, grad["calls"])
+    grad_flop = flops(w.with_tokens(n_loc, n_q=nq_loc))["update"]
+    achieved = grad_flop / (grad_ms / 1e3) / 1e12
+    tok = w.B * (w.n_kv + w.n_q)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, he))
+    line = {"metric": METRIC, "value": tok / (ms_step / 1e3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "dh": w.dh,
+                       "update_tokens_per_head": w.n_kv, "query_tokens_per_head": w.n_q,
+                       "update_tokens_per_rank": n_loc, "query_tokens_per_rank": nq_loc,
+                       "order": w.order, "opt": w.opt,
+                       "parallelism": f"context parallel over {world} ranks (token slices, one all-reduce "
+                                      f"of {cp.buf.nbytes} gradient bytes per update)",
+                       "l2": "inputs larger than L2 (no flush)" if h2d >= 2 * L2_BYTES else "L2 not flushed",
+                       "launch": "direct calls"},
+            "roofline": {"bound": "tensor" if grad["tensor_launches"] > 0 else "alu", "achieved": achieved,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                         "traffic": None, "kernel": "rank 0's slice gradient", "peak_source": f"dense bf16 burst, {pk_src}",
+                         "ms_per_launch": grad_ms, "flop_per_launch": grad_flop},
+            "e2e": {"value": tok / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d * world,
+                    "d2h_bytes_per_step": ho.numel() * ho.element_size() * world, "ms_per_step": e2e_ms},
+            "gpu_launches": launches, "clocks": ck,
+            "phases_ms_per_step": {p_: prof[p_]["ms"] / args.steps for p_ in prof}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w)
+        cb.pop("seconds", None)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     w = li.WORKLOADS[args.workload]
@@ -298,6 +429,8 @@ def main():
         w = dataclasses.replace(w, name=f"{w.name} (reduced: {w.n_kv} update, {w.n_q} query tokens per head)")
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.context_parallel:
+        return run_context_parallel(args, w)
     rank, world, local = dist_env()
     import torch
     from chunk_test_step_b300 import lact as L
