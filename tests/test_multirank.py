@@ -86,3 +86,13 @@ def test_reference_arm_line_has_the_contract_keys():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and "sample" in cb
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_context_parallel_bench_rejects_the_causal_order():
+    # the context-parallel mode spreads one set-order update chunk over the
+    # ranks; a causal layer (a chain of chunks) is refused before any GPU work
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--context-parallel", "--workload", "2"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "set order" in (r.stderr + r.stdout)
