@@ -14,7 +14,9 @@
 //   O_s (TMEM, 128 cols) += U_s . W2[:, r]^T                    (A, B K-major)
 // TMEM holds H_0, H_1, O_0, O_1 (512 columns); H is single-buffered, so the
 // next block's H GEMMs wait until the epilogue has read this block's H out of
-// TMEM (its first step). U is double-buffered in shared memory.
+// TMEM into registers (its first step, before the arithmetic). U is
+// double-buffered in shared memory. The query tiles are requested before the
+// TMEM allocation.
 //
 // Warp roles (320 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer,
 // warps 2..9 epilogue (thread = query row of both subtiles, 32 of the 64
@@ -65,6 +67,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// Packed fp32 pairs (two lanes of work per instruction on sm_100 and later).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 f2_make(float lo, float hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f2 v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+    f2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t pack_f2(f2 v) {
+    float lo, hi;
+    f2_split(v, lo, hi);
+    return pack_bf16(lo, hi);
+}
+
 __device__ __forceinline__ float tanh_approx(float x) {
     float r;
     asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -108,6 +136,15 @@ k_apply2_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         mbar_init(bar(B_O), 1);
         mbar_init(bar(B_DRAIN), 1);
         fence_mbar_init();
+        // the query tiles need no TMEM: their copies start before the allocation
+        if (!skip_cta) {
+            mbar_expect_tx(bar(B_Q), NSUB * NQ * BOX);
+            for (int s = 0; s < NSUB; ++s) {
+                const int tok = (int)(a.t0 + (int64_t)(tile * NSUB + s) * 128);
+                for (int qd = 0; qd < NQ; ++qd)
+                    tma_load_3d(base + OFF_Q + (s * NQ + qd) * BOX, &tm_q, bar(B_Q), qd * 64, tok, bh);
+            }
+        }
     }
     __syncthreads();
     if (skip_cta) return;
@@ -128,12 +165,6 @@ k_apply2_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_expect_tx(bar(B_Q), NSUB * NQ * BOX);
-            for (int s = 0; s < NSUB; ++s) {
-                const int tok = (int)(a.t0 + (int64_t)(tile * NSUB + s) * 128);
-                for (int qd = 0; qd < NQ; ++qd)
-                    tma_load_3d(base + OFF_Q + (s * NQ + qd) * BOX, &tm_q, bar(B_Q), qd * 64, tok, bh);
-            }
             int issued_c = 0, issued_2 = 0;
             bool ok = true;
             for (int r = 0; r < R && ok && !*abort_v; ++r) {
@@ -229,31 +260,39 @@ k_apply2_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const int u = r & 1;
             if (*abort_v || !mbar_wait_warp(bar(B_HF), r & 1, WAIT_NS)) { give_up(); ok = false; break; }
             tc_fence_after();
-            uint32_t pu[NSUB][16];
+            // H leaves TMEM before any arithmetic, so that the next block's H
+            // GEMMs overwrite it while this block's u is computed
+            uint32_t hv[NSUB][2][32];
 #pragma unroll
             for (int s = 0; s < NSUB; ++s) {
-                uint32_t h1[32], h3[32];
-                tmem_ld32(lane_base + COL_H + s * 128 + hf * 32, h1);
-                tmem_ld32(lane_base + COL_H + s * 128 + 64 + hf * 32, h3);
-                tmem_wait_ld();
-                tmem_pin(h1);
-                tmem_pin(h3);
-                // u = silu(h1) h3, with sigmoid(x) = 0.5 tanh(x / 2) + 0.5
+                tmem_ld32(lane_base + COL_H + s * 128 + hf * 32, hv[s][0]);
+                tmem_ld32(lane_base + COL_H + s * 128 + 64 + hf * 32, hv[s][1]);
+            }
+            tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    float uu[2];
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const float x1 = __uint_as_float(h1[j + t]);
-                        const float sg = fmaf(0.5f, tanh_approx(0.5f * x1), 0.5f);
-                        uu[t] = x1 * sg * __uint_as_float(h3[j + t]);
-                    }
-                    pu[s][j / 2] = pack_bf16(uu[0], uu[1]);
-                }
+            for (int s = 0; s < NSUB; ++s) {
+                tmem_pin(hv[s][0]);
+                tmem_pin(hv[s][1]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_HE));
+            // u = silu(h1) h3 with sigmoid(x) = 0.5 tanh(x / 2) + 0.5, two
+            // hidden units per packed fp32 instruction
+            uint32_t pu[NSUB][16];
+            const f2 half2 = f2_make(0.5f, 0.5f);
+#pragma unroll
+            for (int s = 0; s < NSUB; ++s) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const f2 x1 = f2_make(__uint_as_float(hv[s][0][j]), __uint_as_float(hv[s][0][j + 1]));
+                    const f2 x3 = f2_make(__uint_as_float(hv[s][1][j]), __uint_as_float(hv[s][1][j + 1]));
+                    float hx0, hx1;
+                    f2_split(f2_mul(x1, half2), hx0, hx1);
+                    const f2 sg = f2_fma(f2_make(tanh_approx(hx0), tanh_approx(hx1)), half2, half2);
+                    pu[s][j / 2] = pack_f2(f2_mul(f2_mul(x1, sg), x3));
+                }
+            }
             if (r >= 2 && !mbar_wait_warp(bar(B_UE + u), ((r >> 1) - 1) & 1, WAIT_NS)) { give_up(); ok = false; break; }
 #pragma unroll
             for (int s = 0; s < NSUB; ++s) {
