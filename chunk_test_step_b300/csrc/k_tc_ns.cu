@@ -31,7 +31,19 @@
 // G is either the summed gradient or, when the caller skipped the split-K
 // reduction, its partial slots: each CTA then adds its columns' slots in slot
 // order as it reads them (the reduction kernel's order, so the result is the
-// same bit for bit).
+// same bit for bit). The slots come into shared memory by bulk copies (TMA
+// boxes where X is wide), several pieces in flight, before TMEM takes X.
+//
+// With `fuse` set (Muon), the CTA then applies the optimiser step to its part
+// of W itself: W~ = W + scale X (X in W's orientation) and each row of W
+// rescaled to its pre-update norm, W' = W~ ||W_j|| / ||W~_j|| (a row whose
+// updated norm is 0 is stored as updated; a non-finite norm sets
+// ST_NONFINITE), plus W' as bf16. W's tile is copied into the dead Xb during
+// the last iteration; W' leaves by bulk copies. A row of W is a column of X
+// when X is tall (W1, W3: its norm is a sum over the CTA's 128 lanes) and a
+// row of X when X is wide (W2: the CTA's halves and the cluster's CTAs post
+// partial sums, added in rank order, so every CTA finds the same factor).
+// Nothing is written to G then.
 //
 // 256 threads: thread = row of X (TMEM lane) and half of the CTA's columns;
 // thread 0 also issues the MMAs. Every mbarrier wait is bounded and its
@@ -54,7 +66,22 @@ constexpr uint32_t ATOM = M * 128;                 // [128 rows][64 bf16] = 16 K
 constexpr uint32_t OFF_X = 0;                      // n/64 atoms of Xb
 constexpr uint32_t OFF_A = (NMAX / 64) * ATOM;     // 2 atoms of Ab
 constexpr uint32_t OFF_B = OFF_A + 2 * ATOM;       // 2 atoms of Bb
-constexpr uint32_t SMEM_BYTES = OFF_B + 2 * ATOM + 1024;
+// Fused update (after the iterations): W's tile and W' (fp32), W' as bf16,
+// the sums of squares and the row factors.
+constexpr uint32_t OFF_S32 = 0;
+constexpr uint32_t S32_ROW = 1040;                 // X wide: bytes per row (1 KB + 16)
+constexpr uint32_t OFF_S16 = 134144;               // after 128 rows of S32_ROW, 1 KB aligned
+constexpr uint32_t S16_ROW = 528;                  // X wide: bytes per bf16 row (512 + 16)
+constexpr uint32_t OFF_PN = OFF_S16 + M * S16_ROW;
+constexpr uint32_t END_FUSED = OFF_PN + (4 * NMAX * 2 + NMAX) * 4;
+constexpr uint32_t SMEM_BYTES = (END_FUSED > OFF_B + 2 * ATOM ? END_FUSED : OFF_B + 2 * ATOM) + 1024;
+static_assert(OFF_S16 >= M * S32_ROW && 256 * M * 4 <= OFF_S16 && 256 * M * 2 <= M * S16_ROW, "fused update layout");
+// Newton-Schulz input from the split-K partial slots: 16 KB pieces (32
+// columns of X for one half and one slot) in a ring of NPIECE buffers.
+constexpr uint32_t PIECE = M * 128;
+constexpr int NPIECE = 13;
+constexpr int MAXRF = 4;
+static_assert(NPIECE * PIECE <= END_FUSED, "piece ring");
 // TMEM: the CTA's fp32 columns of X at 0 (cb columns); from cb on, A (128)
 // and AA (128), later overwritten by BX (cb).
 constexpr uint32_t COL_X = 0;
@@ -62,6 +89,16 @@ constexpr uint32_t COL_X = 0;
 // Columns of X per CTA for a long side n.
 __host__ __device__ constexpr int ns_block(int n) { return n % 256 == 0 ? 256 : 128; }
 constexpr uint64_t WAIT_NS = 2000000000ull;
+__device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar) : "memory");
+}
 
 struct NsArgs {
     float* g[3];      // gradients in place: W1 [BH,dh,d], W2 [BH,d,dh], W3 [BH,dh,d]
@@ -71,6 +108,13 @@ struct NsArgs {
     int nmat;
     int BH, d, dh, n, steps;
     float a, b, c;
+    // fused update (fuse != 0): in place of writing the result into g, the
+    // step W~ = W + scale X, W' = W~ ||W|| / ||W~|| per row of W, and its
+    // bf16 shadow, are applied here
+    int fuse;
+    float* W[3];
+    bf16* S[3];
+    float scale;
     int* status;
 };
 
@@ -88,7 +132,196 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
     return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
+// Sums over the 32 lanes of a warp, for 32 columns at once: on entry v[c] is
+// this lane's term for column c; on exit v[0] is the warp's sum for column
+// `lane` (recursive halving: 31 shuffles in place of 32 x 5).
+__device__ __forceinline__ void lane_transpose_sum(float (&v)[32], int lane) {
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) {
+        const bool up = (lane & k) != 0;
+#pragma unroll
+        for (int m = 0; m < k; ++m) {
+            const float send = up ? v[m] : v[m + k];
+            const float keep = up ? v[m + k] : v[m];
+            v[m] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+        }
+    }
+}
+
+// The update and row renormalisation of the fast weights, applied to this
+// CTA's columns of the Newton-Schulz result X (fp32 in TMEM), in place of a
+// separate update kernel:
+//   W~ = W + scale X   (X in W's orientation),   W' = W~ ||W_j|| / ||W~_j||
+// for every row j of W (a row whose updated norm is 0 is stored as updated;
+// a non-finite norm sets ST_NONFINITE), and W' also as bf16.
+// The CTA's tile of W arrives in shared memory by bulk copies (issued once the
+// last BX GEMM has read Xb), W~ replaces it there, and W' and its bf16 copy
+// leave by bulk copies: fp32 at OFF_S32, bf16 at OFF_S16, each in W's own
+// row order (X tall: the tile's rows are contiguous in W; X wide: one segment
+// per row, rows padded by 16 bytes so that a warp's rows fall in different banks).
+//  - X tall (W1, W3: rows of W are columns of X): a row of W lies in one CTA;
+//    its norm is a sum over the 128 lanes (threads) of the column.
+//  - X wide (W2: rows of W are rows of X): a row's norm is summed over the
+//    thread's columns, the two halves of the CTA, then the CTAs of the
+//    cluster (each posts its partial sums to all; all add them in rank order).
+// Returns false if a bounded wait ran out.
+__device__ __forceinline__ bool fused_update(const NsArgs& a, int which, int bh, bool tr, int cols, int cs,
+                                             uint32_t rank, int c0, int cb, int half, int row, uint32_t lane_base,
+                                             unsigned char* sm, uint32_t base, float (*upart)[M][2], uint32_t bar_u,
+                                             uint32_t bar_w) {
+    const int tid = threadIdx.x, lane = tid & 31, q = (tid >> 5) & 3;
+    const int hc = cb / 2;
+    float* Wm = a.W[which] + (size_t)bh * a.d * a.dh;
+    bf16* Sm = a.S[which] + (size_t)bh * a.d * a.dh;
+    float* pn = reinterpret_cast<float*>(sm + OFF_PN);        // partial sums of squares
+    float* fs = pn + 4 * NMAX * 2;                            // per-row factors
+    // element (row, column j) of this CTA's block of X, as W stores it
+    auto s32 = [&](int j) -> float* {
+        return tr ? reinterpret_cast<float*>(sm + OFF_S32) + j * M + row
+                  : reinterpret_cast<float*>(sm + OFF_S32 + row * S32_ROW) + j;
+    };
+    if (__syncthreads_and(mbar_wait(bar_w, 0, WAIT_NS) ? 1 : 0) == 0) return false;
+    // pass 1: W~ over W, and the sums of squares of W and W~
+    float p0 = 0.f, p1 = 0.f;
+    for (int h = 0; h < hc / 32; ++h) {
+        const int j0 = half * hc + h * 32;                     // column within the CTA
+        uint32_t v[32];
+        tmem_ld32(lane_base + COL_X + j0, v);
+        tmem_wait_ld();
+        tmem_pin(v);
+        float w[32], s0[32], s1[32];
+        if (tr) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) w[t] = *s32(j0 + t);
+        } else {
+            const float4* wp = reinterpret_cast<const float4*>(s32(j0));
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const float4 x = wp[t];
+                w[4 * t] = x.x; w[4 * t + 1] = x.y; w[4 * t + 2] = x.z; w[4 * t + 3] = x.w;
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            const float tt = fmaf(a.scale, __uint_as_float(v[t]), w[t]);
+            s0[t] = w[t] * w[t];
+            s1[t] = tt * tt;
+            w[t] = tt;
+        }
+        if (tr) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) *s32(j0 + t) = w[t];
+            lane_transpose_sum(s0, lane);
+            lane_transpose_sum(s1, lane);
+            pn[(q * NMAX + j0 + lane) * 2] = s0[0];
+            pn[(q * NMAX + j0 + lane) * 2 + 1] = s1[0];
+        } else {
+            float4* wp = reinterpret_cast<float4*>(s32(j0));
+#pragma unroll
+            for (int t = 0; t < 8; ++t) wp[t] = make_float4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                p0 += s0[t];
+                p1 += s1[t];
+            }
+        }
+    }
+    if (!tr) {
+        pn[(half * M + row) * 2] = p0;
+        pn[(half * M + row) * 2 + 1] = p1;
+    }
+    __syncthreads();
+    bool ok = true;
+    auto factor = [&](float S0, float S1) -> float {
+        const float n0 = sqrtf(S0), n1 = sqrtf(S1);
+        if (!isfinite(n0) || !isfinite(n1)) atomicOr(a.status, ST_NONFINITE);
+        return n1 > 0.f ? n0 / n1 : 1.f;
+    };
+    if (tr) {
+        // column j of X = row c0 + j of W: the four lane quarters' sums
+        for (int j = tid; j < cb; j += NTHREADS) {
+            float S0 = 0.f, S1 = 0.f;
+            for (int k = 0; k < 4; ++k) {
+                S0 += pn[(k * NMAX + j) * 2];
+                S1 += pn[(k * NMAX + j) * 2 + 1];
+            }
+            fs[j] = factor(S0, S1);
+        }
+    } else {
+        // row `tid` of W: the CTA's two halves, posted to every CTA of the
+        // cluster; each posting thread releases its own stores with its arrive
+        if (tid < M) {
+            const float S0 = pn[tid * 2] + pn[(M + tid) * 2], S1 = pn[tid * 2 + 1] + pn[(M + tid) * 2 + 1];
+            for (int r = 0; r < cs; ++r) {
+                st_cluster_f32(mapa_shared(smem_u32(&upart[rank][tid][0]), (uint32_t)r), S0);
+                st_cluster_f32(mapa_shared(smem_u32(&upart[rank][tid][1]), (uint32_t)r), S1);
+                mbar_arrive_cluster(mapa_shared(bar_u, (uint32_t)r));
+            }
+        }
+        ok = __syncthreads_and(mbar_wait_cluster(bar_u, 0, WAIT_NS) ? 1 : 0) != 0;
+        if (ok && tid < M) {
+            float S0 = 0.f, S1 = 0.f;
+            for (int r = 0; r < cs; ++r) {
+                S0 += upart[r][tid][0];
+                S1 += upart[r][tid][1];
+            }
+            fs[tid] = factor(S0, S1);
+        }
+    }
+    __syncthreads();
+    if (!ok) return false;
+    // pass 2: W' = W~ f over W~, and its bf16 copy
+    for (int h = 0; h < hc / 32; ++h) {
+        const int j0 = half * hc + h * 32;
+        float o[32];
+        if (tr) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                o[t] = *s32(j0 + t) * fs[j0 + t];
+                *s32(j0 + t) = o[t];
+                reinterpret_cast<bf16*>(sm + OFF_S16)[(j0 + t) * M + row] = __float2bfloat16_rn(o[t]);
+            }
+        } else {
+            float4* wp = reinterpret_cast<float4*>(s32(j0));
+            const float f = fs[row];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const float4 x = wp[t];
+                o[4 * t] = x.x * f; o[4 * t + 1] = x.y * f; o[4 * t + 2] = x.z * f; o[4 * t + 3] = x.w * f;
+                wp[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+            }
+            uint4* sp = reinterpret_cast<uint4*>(sm + OFF_S16 + row * S16_ROW + j0 * 2);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) sp[t] = pack8(o + 8 * t);
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    // out by bulk copies (the issuing threads wait until shared memory has been read)
+    bool issued = false;
+    if (tr) {
+        const uint32_t w_piece = (uint32_t)(cb * M * 4 / 8), s_piece = (uint32_t)(cb * M * 2 / 8);
+        if (tid < 8) {
+            bulk_store_s2g(Wm + (size_t)c0 * cols + tid * (w_piece / 4), base + OFF_S32 + tid * w_piece, w_piece);
+            issued = true;
+        } else if (tid < 16) {
+            bulk_store_s2g(Sm + (size_t)c0 * cols + (tid - 8) * (s_piece / 2), base + OFF_S16 + (tid - 8) * s_piece,
+                           s_piece);
+            issued = true;
+        }
+    } else if (tid < M) {
+        bulk_store_s2g(Wm + (size_t)tid * cols + c0, base + OFF_S32 + tid * S32_ROW, (uint32_t)(cb * 4));
+        bulk_store_s2g(Sm + (size_t)tid * cols + c0, base + OFF_S16 + tid * S16_ROW, (uint32_t)(cb * 2));
+        issued = true;
+    }
+    if (issued) {
+        bulk_commit();
+        bulk_wait_read0();
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const __grid_constant__ CUtensorMap tm_p, const NsArgs a) {
     pdl_wait();
     pdl_trigger();
     extern __shared__ __align__(16) unsigned char smraw[];
@@ -98,6 +331,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     __shared__ uint32_t tmem_slot;
     __shared__ float red[NTHREADS / 32];
     __shared__ float norm_part[MAXCS];   // partial sums of squares, one per CTA of the cluster
+    __shared__ __align__(8) uint64_t sync_u, sync_w, gbar[MAXRF];
+    __shared__ float upart[MAXCS][M][2];  // fused update: each CTA's row sums of squares (rows spanning the cluster)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = a.n;
@@ -119,6 +354,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         mbar_init(bar, 1);
         mbar_init(bar_a, cs);   // one arrive per CTA of the cluster
         for (int r = 0; r < cs; ++r) mbar_init(barx(r), 1);   // own expect_tx + CTA r's bytes
+        mbar_init(smem_u32(&sync_u), M * cs);   // one arrive per posting thread of each CTA
+        mbar_init(smem_u32(&sync_w), 1);
+        for (int g = 0; g < MAXRF; ++g) mbar_init(smem_u32(&gbar[g]), 1);
         fail_sh = 0;
         fence_mbar_init();
     }
@@ -196,6 +434,73 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     };
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
     float ss = 0.f;
+    bool pre_ok = true;
+    int g_issued = 0, g_waited = 0;     // rounds of pieces started / seen complete (thread 0's drain)
+    const int S = a.slots, rounds = hc / 32, per_round = 2 * S;
+    const int RF = S > 0 ? min(min(rounds, NPIECE / per_round), MAXRF) : 0;
+    if (S > 0) {
+        // The partial slots come into shared memory by bulk copies: a piece
+        // is 32 columns of X for one half and one slot (16 KB); a round is
+        // both halves' pieces of every slot; up to RF rounds are in flight.
+        // Each thread adds its row's values over the slots in slot order.
+        //  - X tall: the piece is 32 whole rows of G (contiguous), read
+        //    [column][row] by the threads;
+        //  - X wide: a TMA box of 128 rows x 32 columns, 128-byte swizzled.
+        const float* P0 = a.part + (size_t)which * a.mat + (size_t)bh * a.d * a.dh;
+        const size_t sstride = (size_t)a.nmat * a.mat;
+        auto issue_round = [&](int k) {
+            const int g = k % RF;
+            const uint32_t gb = smem_u32(&gbar[g]);
+            mbar_expect_tx(gb, (uint32_t)per_round * PIECE);
+            for (int h = 0; h < 2; ++h)
+                for (int sl = 0; sl < S; ++sl) {
+                    const uint32_t dst = base + (uint32_t)(g * per_round + h * S + sl) * PIECE;
+                    const int jc = c0 + h * hc + 32 * k;           // first column of X in the piece
+                    if (tr) bulk_load_g2s(dst, P0 + sl * sstride + (size_t)jc * cols, PIECE, gb);
+                    else tma_load_2d(dst, &tm_p, gb, jc, ((sl * a.nmat + which) * a.BH + bh) * M);
+                }
+        };
+        if (tid == 0) {
+            prefetch_tmap(&tm_p);
+            for (int k = 0; k < RF; ++k) issue_round(k);
+            g_issued = RF;
+        }
+        for (int k = 0; k < rounds; ++k) {
+            const int g = k % RF;
+            pre_ok = __syncthreads_and(mbar_wait(smem_u32(&gbar[g]), (uint32_t)((k / RF) & 1), WAIT_NS) ? 1 : 0) != 0;
+            if (!pre_ok) break;
+            g_waited = k + 1;
+            float x[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) x[t] = 0.f;
+            for (int sl = 0; sl < S; ++sl) {
+                const unsigned char* pc = sm + (uint32_t)(g * per_round + half * S + sl) * PIECE;
+                if (tr) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) x[t] += reinterpret_cast<const float*>(pc)[t * M + row];
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 y = *reinterpret_cast<const float4*>(pc + row * 128 + ((c ^ (row & 7)) << 4));
+                        x[4 * c] += y.x; x[4 * c + 1] += y.y; x[4 * c + 2] += y.z; x[4 * c + 3] += y.w;
+                    }
+                }
+            }
+            uint32_t v[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                ss = fmaf(x[t], x[t], ss);
+                v[t] = __float_as_uint(x[t]);
+            }
+            tmem_st32(lane_base + COL_X + half * hc + 32 * k, v);
+            __syncthreads();                       // round k's buffers are read
+            if (tid == 0 && k + RF < rounds) {
+                fence_proxy_async_smem();
+                issue_round(k + RF);
+                g_issued = k + RF + 1;
+            }
+        }
+    } else {
     for (int h = 0; h < hc / 32; h += 2) {
         // two 32-column pieces in flight at once
         float x0[32], x1[32];
@@ -215,6 +520,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
         }
         tmem_st32(lane_base + COL_X + half * hc + h * 32 + 32, v);
     }
+    }
     tmem_wait_st();
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) red[warp] = ss;
@@ -227,7 +533,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
             mbar_arrive_cluster(mapa_shared(bar_a, (uint32_t)r));
         }
     }
-    bool ok = __syncthreads_and(mbar_wait_cluster(bar_a, 0, WAIT_NS) ? 1 : 0) != 0;
+    bool ok = __syncthreads_and(mbar_wait_cluster(bar_a, 0, WAIT_NS) ? 1 : 0) != 0 && pre_ok;
     float tot = 0.f;
     for (int r = 0; r < cs; ++r) tot += norm_part[r];
     const float inv = 1.0f / (sqrtf(tot) + 1e-7f);
@@ -277,6 +583,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     // then after iteration n-1) is consumed by the A GEMM of iteration n, with
     // parity n & 1. Thread 0 sets up the count of each incoming send.
     int sends = 0;                 // sends expected (thread 0's count)
+    bool w_issued = false;         // the fused update's copies of W's tile were started
     int waited[MAXCS] = {0, 0, 0, 0};
     auto expect_columns = [&]() {
         if (tid == 0) {
@@ -412,11 +719,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
                     mma_bf16(tmem + COL_BX, dB + ko, dXmn + xo + j * 128, i_bx, j > 0 ? 1u : 0u);
                 }
                 mma_commit(bar);
+                if (a.fuse && it + 1 == a.steps) mbar_expect_tx(smem_u32(&sync_w), (uint32_t)(cb * M * 4));
             }
             if (!mma_done()) ok = false;
         }
         // no CTA still reads Xb with its A GEMM
         if (!cluster_wait(bar_a, (it + 1) & 1)) ok = false;
+        // fused update, last iteration: every CTA's A GEMM is over (so the bulk
+        // copies out of this Xb have landed) and the BX GEMM has read it, so
+        // the CTA's tile of W comes into that space while X gets its last update
+        if (ok && a.fuse && it + 1 == a.steps) {
+            w_issued = true;
+            const float* Wp = a.W[which] + (size_t)bh * a.d * a.dh;
+            if (tr) {
+                if (tid < 8)
+                    bulk_load_g2s(base + OFF_S32 + tid * (cb * M * 4 / 8), Wp + (size_t)c0 * cols + tid * (cb * M / 8),
+                                  (uint32_t)(cb * M * 4 / 8), smem_u32(&sync_w));
+            } else if (tid < M) {
+                bulk_load_g2s(base + OFF_S32 + tid * S32_ROW, Wp + (size_t)tid * cols + c0, (uint32_t)(cb * 4),
+                              smem_u32(&sync_w));
+            }
+        }
         if (ok) {
             // X_j = a X_j + BX_j in TMEM; bf16(X_j) into this CTA's block of Xb
             for (int h = 0; h < hc / 32; h += 2) {
@@ -443,6 +766,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
                         vx[u][t] = __float_as_uint(xn[t]);
                     }
                     tmem_st32(lane_base + COL_X + j0, vx[u]);
+                    if (a.fuse && it + 1 == a.steps) continue;   // Xb holds W's tile now
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         *reinterpret_cast<uint4*>(sm + OFF_X + atom_off(row, c0 + j0 + 8 * c)) = pack8(xn + 8 * c);
@@ -460,7 +784,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
     }
     if (!ok) {
         if (tid == 0) atomicOr(a.status, ST_TIMEOUT);
-    } else {
+    } else if (!a.fuse) {
         // this CTA's columns back into G's own orientation
         for (int h = 0; h < hc / 32; ++h) {
             const int j0 = half * hc + h * 32;
@@ -479,11 +803,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_ns_tc(const NsArgs a) {
                                                                     __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3]));
             }
         }
+    } else {
+        ok = fused_update(a, which, bh, tr, cols, cs, rank, c0, cb, half, row, lane_base, sm, base, upart,
+                          smem_u32(&sync_u), smem_u32(&sync_w));
+        if (!ok && tid == 0) atomicOr(a.status, ST_TIMEOUT);
     }
     // every MMA has completed once this commit lands (bounded drain); after
     // an early exit from the loop, columns still on their way in are waited
     // for (bounded) before the CTA may leave
     if (tid == 0) {
+        if (w_issued) mbar_wait(smem_u32(&sync_w), 0, WAIT_NS);   // W's tile copies have landed
+        for (int k = g_waited; k < g_issued; ++k) mbar_wait(smem_u32(&gbar[k % RF]), (uint32_t)((k / RF) & 1), WAIT_NS);
         mma_commit(bar);
         mbar_wait(bar, phase & 1, WAIT_NS);
         for (int r = 0; r < cs; ++r)
@@ -509,9 +839,16 @@ bool ns_tc_supported(const lact_state* st) {
     return st->cfg.io_dtype == LACT_BF16 && m == M && n <= NMAX && n % 128 == 0;
 }
 
-cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], int slots, cudaStream_t s) {
+cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], int slots, bool fuse_update, cudaStream_t s) {
     NsArgs a;
-    for (int m = 0; m < 3; ++m) a.g[m] = static_cast<float*>(g[m]);
+    for (int m = 0; m < 3; ++m) {
+        a.g[m] = static_cast<float*>(g[m]);
+        a.W[m] = static_cast<float*>(st->W[m]);
+        a.S[m] = st->Wsh[m];
+    }
+    if (slots < 0 || slots > kNsFusedSlots) return cudaErrorInvalidValue;   // the piece ring holds a round of 4
+    a.fuse = fuse_update ? 1 : 0;
+    a.scale = (float)-st->cfg.muon_lr;
     a.part = static_cast<const float*>(st->partial);
     a.slots = slots;
     a.mat = (size_t)st->BH * st->cfg.d * st->cfg.dh;
@@ -528,6 +865,14 @@ cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], int slots, cuda
     cudaError_t e = cudaFuncSetAttribute(k_ns_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int cs = a.n / ns_block(a.n);
+    // the partial slots as rows of n fp32 (each matrix of each slot: 128 rows)
+    CUtensorMap tm_p;
+    {
+        const uint64_t dims[2] = {(uint64_t)a.n, (uint64_t)kMaxSlots * st->nmat * st->BH * M};
+        const uint64_t str[1] = {(uint64_t)a.n * 4};
+        const uint32_t box[2] = {32, M};
+        if (!make_tmap_2d(&tm_p, st->partial, true, dims, str, box)) return cudaErrorInvalidValue;
+    }
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)(cs * st->nmat * st->BH));
     lc.blockDim = dim3(NTHREADS);
@@ -542,10 +887,11 @@ cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], int slots, cuda
     at[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = at;
     lc.numAttrs = 2;
-    e = cudaLaunchKernelEx(&lc, k_ns_tc, a);
+    e = cudaLaunchKernelEx(&lc, k_ns_tc, tm_p, a);
     g_launches++;
     g_tc_launches++;
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace lact
+

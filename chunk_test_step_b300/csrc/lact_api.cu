@@ -194,9 +194,13 @@ static lact_status do_step(lact_state* st, void* const g[3], cudaStream_t s, int
     double scale = -1.0;
     if (st->cfg.opt == LACT_OPT_MUON) {
         PhaseTimer t(st, LACT_PHASE_NS, s);
-        cudaError_t e = ns_tc_supported(st) ? launch_ns_tc(st, g, slots, s) : launch_newton_schulz(st, g, s);
+        // on the tensor cores, Newton-Schulz applies the update + renorm to
+        // its result itself (no update launch)
+        const bool tc = ns_tc_supported(st);
+        cudaError_t e = tc ? launch_ns_tc(st, g, slots, true, s) : launch_newton_schulz(st, g, s);
         t.done();
         if (e != cudaSuccess) return LACT_ERR_CUDA;
+        if (tc) return LACT_OK;
         scale = -st->cfg.muon_lr;
     }
     PhaseTimer t(st, LACT_PHASE_UPDATE, s);

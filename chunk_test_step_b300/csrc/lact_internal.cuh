@@ -160,16 +160,20 @@ cudaError_t launch_grad_simt(const lact_state* st, TokView k, TokView v, const f
 bool tmap_available();
 bool make_tmap_bf16(CUtensorMap* m, const void* p, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                     const uint32_t* box);
+bool make_tmap_2d(CUtensorMap* m, const void* p, bool f32, const uint64_t* dims, const uint64_t* strides_bytes,
+                  const uint32_t* box);
 
 // Tensor-core (tcgen05) path: bf16 io, d = 128, dh a multiple of 64.
 bool grad_tc_supported(const lact_state* st);
 cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots_used,
                            cudaStream_t s);
 bool ns_tc_supported(const lact_state* st);
-// Newton-Schulz in place on g[]. With slots > 0 the gradient is not in g[]
-// yet: the kernel adds the split-K partial slots 0 .. slots-1 (in that order,
-// as launch_reduce does) while it reads them, and writes its result to g[].
-cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], int slots, cudaStream_t s);
+// Newton-Schulz on the gradient in g[]. With slots > 0 the gradient is not in
+// g[] yet: the kernel adds the split-K partial slots 0 .. slots-1 (in that
+// order, as launch_reduce does) while it reads them. Without fuse_update the
+// result overwrites g[]; with it, the Muon step and row renorm are applied to
+// the state's W (and bf16 shadow) from the result, and g[] is left as it was.
+cudaError_t launch_ns_tc(const lact_state* st, void* const g[3], int slots, bool fuse_update, cudaStream_t s);
 // Most split-K slots Newton-Schulz adds up itself (more go through launch_reduce).
 constexpr int kNsFusedSlots = 4;
 bool apply_tc_supported(const lact_state* st);

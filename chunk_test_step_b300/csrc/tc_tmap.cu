@@ -41,4 +41,17 @@ bool make_tmap_bf16(CUtensorMap* m, const void* p, int rank, const uint64_t* dim
     return r == CUDA_SUCCESS;
 }
 
+// 2D fp32 (f32 = true) or bf16 map, 128-byte swizzle.
+bool make_tmap_2d(CUtensorMap* m, const void* p, bool f32, const uint64_t* dims, const uint64_t* strides_bytes,
+                  const uint32_t* box) {
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t gd[2] = {dims[0], dims[1]}, gs[1] = {strides_bytes[0]};
+    cuuint32_t bx[2] = {box[0], box[1]}, es[2] = {1, 1};
+    CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void*>(p), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace lact
