@@ -32,15 +32,18 @@ def _layer(w, inp, max_chunk=None):
     return L.LactLayer(config_for(w, max_chunk), to_device(inp.W1), to_device(inp.W2), to_device(inp.W3))
 
 
-@pytest.mark.parametrize("num", [4, 1])
-def test_zero_weight_row_stays_zero(num):
+@pytest.mark.parametrize("num,mat", [(4, 0), (1, 0), (4, 1), (8, 1)])
+def test_zero_weight_row_stays_zero(num, mat):
+    # mat 0: a row of W1 (for Muon on the tensor cores a column of Newton-Schulz's
+    # tall X, normed over the lanes); mat 1: a row of W2 (a row of the wide X,
+    # normed across the cluster's CTAs)
     import torch
     from chunk_test_step_b300 import lact as L
     w = li.WORKLOADS[num].with_tokens(1000 + 37, seed=li.WORKLOADS[num].seed + 8000)
     inp = li.make_inputs(w)
-    W1 = inp.W1.copy()
-    W1[:, 5, :] = 0.0                       # hidden unit 5 of every head: W1 row of zeros
-    inp = dataclasses.replace(inp, W1=W1)
+    Wz = (inp.W1 if mat == 0 else inp.W2).copy()
+    Wz[:, 5, :] = 0.0                       # row 5 of every head's matrix: zeros
+    inp = dataclasses.replace(inp, **{"W1" if mat == 0 else "W2": Wz})
     n = w.n_kv
     layer = _layer(w, inp, max_chunk=n)
     k, v, e = to_device(inp.k), to_device(inp.v), to_device(inp.eta)
@@ -48,13 +51,13 @@ def test_zero_weight_row_stays_zero(num):
     got = [to_host_f64(x) for x in layer.weights()]
     torch.cuda.synchronize()
     assert L.lact_sync_status(layer.handle) == L.LACT_OK
-    assert np.all(got[0][:, :, 5, :] == 0.0)
+    assert np.all(got[mat][:, :, 5, :] == 0.0)
     for b in range(w.B):
         for h in range(w.H):
             Wf = O.chunk_update(tuple(x[h].astype(np.float64) for x in (inp.W1, inp.W2, inp.W3)),
                                 li.as_f64(inp.k[b, h]), li.as_f64(inp.v[b, h]), inp.eta[b, h].astype(np.float64),
                                 w.opt, lr=w.muon_lr, ns_steps=w.ns_steps)
-            assert np.all(Wf[0][5] == 0.0)
+            assert np.all(Wf[mat][5] == 0.0)
             for m in range(3):
                 err = np.linalg.norm(got[m][b, h] - Wf[m]) / np.linalg.norm(Wf[m])
                 record("zero_row", w, "W%d" % (m + 1), err, TOL[w.dtype], b=b, h=h)
@@ -92,6 +95,12 @@ CORNERS = [
     (32, 64, "f32", "muon"),
     (256, 1024, "f32", "gd"),
     (128, 1024, "f32", "muon"),
+    # Newton-Schulz on the tensor cores with the update inside, at the other
+    # long sides it serves: n = 256 (one 256-column CTA), n = 384 (a cluster
+    # of three 128-column CTAs), and W1/W3 wide with W2 tall (d > dh)
+    (128, 256, "bf16", "muon"),
+    (128, 384, "bf16", "muon"),
+    (256, 128, "bf16", "muon"),
 ]
 
 
@@ -185,3 +194,20 @@ def test_two_states_on_two_streams_run_independently():
     for a, b in zip(seq, conc):
         for x, y in zip(a, b):
             assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("mat", [0, 1])
+def test_nonfinite_weight_sets_status_in_the_fused_muon_step(mat):
+    # a NaN in W1 (tall) or W2 (wide) on the bf16 Muon layer: Newton-Schulz's
+    # own update finds a non-finite row norm and sets the sticky status
+    import torch
+    from chunk_test_step_b300 import lact as L
+    w = li.WORKLOADS[4].with_tokens(256, seed=li.WORKLOADS[4].seed + 8500)
+    inp = li.make_inputs(w)
+    layer = _layer(w, inp, max_chunk=w.n_kv)
+    Ws = list(layer.weights())
+    Ws[mat][0, 0, 3, 5] = float("nan")
+    L.lact_set_weights(layer.handle, *Ws)
+    k, v, e = to_device(inp.k), to_device(inp.v), to_device(inp.eta)
+    L.lact_chunk_update(layer.handle, k, v, e, w.n_kv)
+    assert L.lact_sync_status(layer.handle) == L.LACT_ERR_NONFINITE
