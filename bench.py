@@ -108,8 +108,8 @@ def tokens_per_step(w: li.Workload) -> int:
 # token splits): reads (K, V, eta) grow with the tokens (x 8), writes (the
 # split-K partial sums) with the splits (23 at full size). It describes the
 # kernel source it was taken on, identified by its hash.
-GRAD_TRAFFIC = {"workload": 5, "bytes": 560205824 * 8 + 46391808 * 23 // 9, "kernel_source": "k_tc_grad.cu",
-                "sha256_prefix": "83ae3cd43ad83ce0"}
+GRAD_TRAFFIC = {"workload": 5, "bytes": 560231168 * 8 + 46721536 * 23 // 9, "kernel_source": "k_tc_grad.cu",
+                "sha256_prefix": "595c084a655bb093"}
 
 
 def measured_traffic(w: li.Workload, reduced: bool):

@@ -454,7 +454,7 @@ bool grad_tc_supported(const lact_state* st) {
 }
 
 cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots,
-                           cudaStream_t s) {
+                           double side_tiles, cudaStream_t s) {
     const int dh = st->cfg.dh, BH = st->BH;
     CUtensorMap mk, mv, m1, m3, m2;
     const uint64_t kv_dims[3] = {(uint64_t)D, (uint64_t)k.n_total, (uint64_t)BH};
@@ -477,11 +477,15 @@ cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const flo
     const int ntiles = (int)((k.n + TT - 1) / TT);
     const int units = BH * (dh / HB);
     // Token splits (one CTA per SM; each split writes one fp32 partial per
-    // unit that the reduction reads back). Cost in units of one tile's time:
-    // waves x (tiles per CTA + ~3 tiles of pipeline fill and drain per CTA)
-    // + ~0.5 per split for writing and re-reading its partial sums. This picks
-    // one long wave where the grid allows (e.g. 48 units x 3 splits on 148
-    // SMs) and whole waves of shorter CTAs otherwise.
+    // unit that the reduction or Newton-Schulz reads back). Cost in units of
+    // one tile's time: waves x (tiles per CTA + ~3 tiles of pipeline fill and
+    // drain per CTA); when other work shares the GPU (side_tiles, e.g. the
+    // chunk's readout beside it in the causal order) it takes the SMs a short
+    // last wave leaves idle, so the phase ends no earlier than the SM-time of
+    // both over the SM count; + ~0.5 per split for writing and re-reading
+    // its partial sums. This picks one long wave where the grid allows (e.g. 48
+    // units x 3 splits on 148 SMs), whole waves of shorter CTAs otherwise,
+    // and few splits when a readout fills the gaps.
     int splits = 1;
     double best = 1e30;
     for (int sp = 1; sp <= kMaxSlots && sp <= ntiles; ++sp) {
@@ -490,7 +494,9 @@ cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const flo
         if (used != sp) continue;
         const int64_t ctas = (int64_t)units * sp;
         const int64_t waves = (ctas + st->num_sms - 1) / st->num_sms;
-        const double cost = (double)waves * (tps + 3.0) + 0.5 * sp;
+        const double path = (double)waves * (tps + 3.0);
+        const double shared = side_tiles > 0 ? ((double)ctas * (tps + 3.0) + side_tiles) / st->num_sms : 0.0;
+        const double cost = (path > shared ? path : shared) + 0.5 * sp;
         if (cost < best - 1e-9) { best = cost; splits = sp; }
     }
     const int tps = (ntiles + splits - 1) / splits;

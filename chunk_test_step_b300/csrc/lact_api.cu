@@ -143,7 +143,7 @@ static lact_status do_apply(lact_state* st, TokView q, void* o, cudaStream_t s) 
 // over: when the tensor-core Newton-Schulz will run and the partial slots are
 // few, the reduction is skipped and *deferred holds their count (else 0).
 static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* eta, bool accumulate,
-                           void* const out[3], cudaStream_t s, int* deferred = nullptr) {
+                           void* const out[3], cudaStream_t s, int* deferred = nullptr, double side_tiles = 0.0) {
     if (deferred) *deferred = 0;
     if (k.n == 0) {
         if (!accumulate) {
@@ -171,7 +171,7 @@ static lact_status do_grad(lact_state* st, TokView k, TokView v, const float* et
         PhaseTimer t(st, LACT_PHASE_GRAD, s);
         cudaError_t e = st->nmat == 1        ? (lin_tc_supported(st) ? launch_lin_grad_tc(st, k, v, eta, &slots, s)
                                                                      : launch_lin_grad_simt(st, k, v, eta, &slots, s))
-                        : grad_tc_supported(st) ? launch_grad_tc(st, k, v, eta, &slots, s)
+                        : grad_tc_supported(st) ? launch_grad_tc(st, k, v, eta, &slots, side_tiles, s)
                                                 : launch_grad_simt(st, k, v, eta, &slots, s);
         t.done();
         if (e != cudaSuccess) return LACT_ERR_CUDA;
@@ -387,7 +387,12 @@ lact_status lact_sequence(lact_state* st, lact_order order, const void* d_q, int
             if (r != LACT_OK) return r;
             if (cudaEventRecord(st->ev_join, st->side) != cudaSuccess) return LACT_ERR_CUDA;
             int deferred = 0;
-            r = do_grad(st, TokView{d_k, n_kv, t0, n}, TokView{d_v, n_kv, t0, n}, d_eta, false, st->dW, s, &deferred);
+            // the readout's share of the GPU beside the gradient, in tile-times of
+            // the gradient kernel: a CTA per 256 queries and head takes about one
+            // tile-time per 64 hidden units (measured on the 3B-shaped layer)
+            const double side = (double)((n + 255) / 256) * st->BH * (st->cfg.dh / 64);
+            r = do_grad(st, TokView{d_k, n_kv, t0, n}, TokView{d_v, n_kv, t0, n}, d_eta, false, st->dW, s, &deferred,
+                        side);
             if (r != LACT_OK) return r;
             if (cudaStreamWaitEvent(s, st->ev_join, 0) != cudaSuccess) return LACT_ERR_CUDA;
             r = do_step(st, st->dW, s, deferred);

@@ -166,7 +166,7 @@ bool make_tmap_2d(CUtensorMap* m, const void* p, bool f32, const uint64_t* dims,
 // Tensor-core (tcgen05) path: bf16 io, d = 128, dh a multiple of 64.
 bool grad_tc_supported(const lact_state* st);
 cudaError_t launch_grad_tc(const lact_state* st, TokView k, TokView v, const float* eta, int* slots_used,
-                           cudaStream_t s);
+                           double side_tiles, cudaStream_t s);
 bool ns_tc_supported(const lact_state* st);
 // Newton-Schulz on the gradient in g[]. With slots > 0 the gradient is not in
 // g[] yet: the kernel adds the split-K partial slots 0 .. slots-1 (in that
