@@ -155,7 +155,7 @@ __device__ __forceinline__ void lane_transpose_sum(float (&v)[32], int lane) {
 // for every row j of W (a row whose updated norm is 0 is stored as updated;
 // a non-finite norm sets ST_NONFINITE), and W' also as bf16.
 // The CTA's tile of W arrives in shared memory by bulk copies (issued once the
-// last BX GEMM has read Xb), W~ replaces it there, and W' and its bf16 copy
+// last BX GEMM has read Xb), W~ replaces X in TMEM, and W' and its bf16 copy
 // leave by bulk copies: fp32 at OFF_S32, bf16 at OFF_S16, each in W's own
 // row order (X tall: the tile's rows are contiguous in W; X wide: one segment
 // per row, rows padded by 16 bytes so that a warp's rows fall in different banks).
@@ -206,19 +206,15 @@ __device__ __forceinline__ bool fused_update(const NsArgs& a, int which, int bh,
             const float tt = fmaf(a.scale, __uint_as_float(v[t]), w[t]);
             s0[t] = w[t] * w[t];
             s1[t] = tt * tt;
-            w[t] = tt;
+            v[t] = __float_as_uint(tt);
         }
+        tmem_st32(lane_base + COL_X + j0, v);       // W~ over X in TMEM
         if (tr) {
-#pragma unroll
-            for (int t = 0; t < 32; ++t) *s32(j0 + t) = w[t];
             lane_transpose_sum(s0, lane);
             lane_transpose_sum(s1, lane);
             pn[(q * NMAX + j0 + lane) * 2] = s0[0];
             pn[(q * NMAX + j0 + lane) * 2 + 1] = s1[0];
         } else {
-            float4* wp = reinterpret_cast<float4*>(s32(j0));
-#pragma unroll
-            for (int t = 0; t < 8; ++t) wp[t] = make_float4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
                 p0 += s0[t];
@@ -226,6 +222,7 @@ __device__ __forceinline__ bool fused_update(const NsArgs& a, int which, int bh,
             }
         }
     }
+    tmem_wait_st();
     if (!tr) {
         pn[(half * M + row) * 2] = p0;
         pn[(half * M + row) * 2 + 1] = p1;
@@ -270,26 +267,36 @@ __device__ __forceinline__ bool fused_update(const NsArgs& a, int which, int bh,
     }
     __syncthreads();
     if (!ok) return false;
-    // pass 2: W' = W~ f over W~, and its bf16 copy
+    // pass 2: W' = W~ f (W~ from TMEM) into the stage, and its bf16 copy
     for (int h = 0; h < hc / 32; ++h) {
         const int j0 = half * hc + h * 32;
+        uint32_t v[32];
+        tmem_ld32(lane_base + COL_X + j0, v);
+        tmem_wait_ld();
+        tmem_pin(v);
         float o[32];
         if (tr) {
+            const float4* fp = reinterpret_cast<const float4*>(fs + j0);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const float4 f4 = fp[t];
+                o[4 * t] = __uint_as_float(v[4 * t]) * f4.x;
+                o[4 * t + 1] = __uint_as_float(v[4 * t + 1]) * f4.y;
+                o[4 * t + 2] = __uint_as_float(v[4 * t + 2]) * f4.z;
+                o[4 * t + 3] = __uint_as_float(v[4 * t + 3]) * f4.w;
+            }
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
-                o[t] = *s32(j0 + t) * fs[j0 + t];
                 *s32(j0 + t) = o[t];
                 reinterpret_cast<bf16*>(sm + OFF_S16)[(j0 + t) * M + row] = __float2bfloat16_rn(o[t]);
             }
         } else {
-            float4* wp = reinterpret_cast<float4*>(s32(j0));
             const float f = fs[row];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const float4 x = wp[t];
-                o[4 * t] = x.x * f; o[4 * t + 1] = x.y * f; o[4 * t + 2] = x.z * f; o[4 * t + 3] = x.w * f;
-                wp[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
-            }
+            for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(v[t]) * f;
+            float4* wp = reinterpret_cast<float4*>(s32(j0));
+#pragma unroll
+            for (int t = 0; t < 8; ++t) wp[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
             uint4* sp = reinterpret_cast<uint4*>(sm + OFF_S16 + row * S16_ROW + j0 * 2);
 #pragma unroll
             for (int t = 0; t < 4; ++t) sp[t] = pack8(o + 8 * t);
