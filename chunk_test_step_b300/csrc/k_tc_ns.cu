@@ -181,7 +181,7 @@ __device__ __forceinline__ bool fused_update(const NsArgs& a, int which, int bh,
                   : reinterpret_cast<float*>(sm + OFF_S32 + row * S32_ROW) + j;
     };
     if (__syncthreads_and(mbar_wait(bar_w, 0, WAIT_NS) ? 1 : 0) == 0) return false;
-    // pass 1: W~ over W, and the sums of squares of W and W~
+    // pass 1: W~ (into TMEM over X), and the sums of squares of W and W~
     float p0 = 0.f, p1 = 0.f;
     for (int h = 0; h < hc / 32; ++h) {
         const int j0 = half * hc + h * 32;                     // column within the CTA
