@@ -99,7 +99,9 @@ typedef enum {
     LACT_PHASE_GRAD = 1,     /* chunk gradient: the fused kernel (head dim 128), or per token
                                 slice the per-token kernel + weight-gradient GEMMs (256) */
     LACT_PHASE_REDUCE = 2,   /* split-K partial-sum reduction */
-    LACT_PHASE_NS = 3,       /* Newton-Schulz (Muon) */
+    LACT_PHASE_NS = 3,       /* Newton-Schulz (Muon); on the tensor cores (bf16 io, short
+                                side 128) the same kernel also applies the update, row
+                                renorm and bf16 shadow, and UPDATE then has no calls */
     LACT_PHASE_UPDATE = 4,   /* update + row renorm + bf16 shadow */
     LACT_NUM_PHASES = 5
 } lact_phase;
