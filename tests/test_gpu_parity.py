@@ -484,8 +484,13 @@ def test_sequence_replayed_from_a_cuda_graph_matches_direct_calls(num):
     assert max(errs.values()) < TOL[w.dtype], errs
 
 
-@pytest.mark.parametrize("num,n", [(4, 5000 + 13), (8, 4096), (5, 8192 + 77), (10, 3000)])
-def test_update_equals_gradient_then_apply_gradient(num, n):
+# (workload, tokens, heads): the token splits the gradient picks here are 3
+# (workload 4, and 8 at 4,096 tokens), 2 (5), 4 (4 heads of workload 4 at
+# 3,072 tokens) and 1 (workload 8 at 256 tokens): Newton-Schulz reads that many
+# partial slots, in rounds of pieces whose depth depends on the count
+@pytest.mark.parametrize("num,n,heads", [(4, 5000 + 13, None), (8, 4096, None), (5, 8192 + 77, None), (10, 3000, None),
+                                         (4, 3072, 4), (8, 256, None)])
+def test_update_equals_gradient_then_apply_gradient(num, n, heads):
     # One update (gradient, its split-K sum, Muon step, renorm) against the
     # same done as two calls: lact_chunk_gradient (the sum by the reduction
     # kernel) then lact_apply_gradient. With few token splits the update lets
@@ -494,10 +499,17 @@ def test_update_equals_gradient_then_apply_gradient(num, n):
     torch = _torch()
     from chunk_test_step_b300 import lact as L
     w = li.WORKLOADS[num].with_tokens(n, seed=li.WORKLOADS[num].seed + 7000)
+    if heads is not None:
+        w = dataclasses.replace(w, H=heads)
     inp = li.make_inputs(w)
     k, v, e = to_device(inp.k), to_device(inp.v), to_device(inp.eta)
     one = _layer(w, inp, max_chunk=n)
+    L.lact_set_profiling(one.handle, True)
     L.lact_chunk_update(one.handle, k, v, e, n)
+    if heads is not None or n == 256:
+        # the cases picked for their 4 and 1 token splits: Newton-Schulz added
+        # the slots itself (no reduction launch)
+        assert L.lact_get_profile(one.handle)["reduce"]["calls"] == 0
     two = _layer(w, inp, max_chunk=n)
     shapes = ((w.d, w.d),) if w.memory == "linear" else ((w.dh, w.d), (w.d, w.dh), (w.dh, w.d))
     g = [torch.empty(w.B, w.H, *s, device="cuda") for s in shapes] + [None] * (3 - len(shapes))
