@@ -101,6 +101,10 @@ CORNERS = [
     (128, 256, "bf16", "muon"),
     (128, 384, "bf16", "muon"),
     (256, 128, "bf16", "muon"),
+    # the tensor-core path's smallest hidden sizes: two blocks of 64 with all
+    # three Newton-Schulz matrices square, and a single block
+    (128, 128, "bf16", "muon"),
+    (128, 64, "bf16", "gd"),
 ]
 
 
